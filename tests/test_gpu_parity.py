@@ -1,0 +1,204 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Bit-exact: commit windows, committed conv history, untouched slots, the pool
+after verify, device status codes.  Everything else (xc, o, replay rows,
+committed state) within a max relative error of 1e-4, floored at 0.1 x the
+RMS of the reference tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_workloads as W
+from gpu_harness import (TOL, Batch, GpuPools, batch_from, compare, relerr, run_gpu, run_oracle)
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU machines, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def check_commit(b: Batch, pools: GpuPools, ref_ssm, ref_hist, before_ssm, before_hist):
+    ssm = pools.ssm.cpu().numpy()
+    hist = pools.conv_hist.cpu().numpy()
+    committed = sorted({int(b.slot_map[s]) for s in range(b.S) if b.accepted[s] >= 0})
+    others = sorted(set(range(b.P)) - set(committed))
+    assert np.array_equal(hist, ref_hist), "conv history after commit differs"
+    assert np.array_equal(ssm[others], before_ssm[others]), "an untouched slot changed"
+    err = 0.0
+    if committed:
+        err = relerr(ssm[committed], ref_ssm[committed])
+        assert err <= TOL, err
+    return err
+
+
+def run_rounds(sp: W.Spec, rounds, layer=0, max_nodes=None):
+    """Rounds of conv -> verify -> commit; each side carries its own pools."""
+    lp = W.layer_params(sp, layer)
+    sm = W.slot_map(sp)
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    ssm, hist = lp.ssm.copy(), lp.conv_hist.copy()
+    worst = {}
+    for r in rounds:
+        ri = W.round_inputs(sp, layer, r)
+        b = batch_from(sp, lp, ri, sm, max_nodes)
+        gpu_before = pools.ssm.cpu().numpy()
+        g = run_gpu(b, pools)
+        ref = run_oracle(b, ssm, hist)
+        errs = compare(g, ref)
+        errs["ssm"] = check_commit(b, pools, ref.ssm, ref.conv_hist, gpu_before, hist)
+        ssm, hist = ref.ssm, ref.conv_hist
+        for k, v in errs.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    return worst
+
+
+@pytest.mark.parametrize("cfg,rounds", [(0, 1), (1, 32), (2, 32)])
+def test_small_configs_all_rounds(cfg, rounds):
+    """Tiny, chain-of-8 and four 16-node trees: every round, pools carried over."""
+    worst = run_rounds(W.spec(cfg), range(rounds))
+    print(cfg, {k: f"{v:.2e}" for k, v in worst.items()})
+
+
+def test_layer_stack_sampled_layers():
+    """48-layer stack (5 sequences of {4,8,12,16,16} nodes, grouped 3:1):
+    round 0 of a sample of layers, each with its own weights and pools."""
+    sp = W.spec(3)
+    for layer in (0, 13, 31, 47):
+        run_rounds(sp, [0], layer=layer)
+
+
+@pytest.mark.parametrize("variant", W.SWEEP_VARIANTS)
+def test_sweep_full_size_sampled(variant):
+    """The benchmark's workload at full size (64 sequences, 128-slot pool), in
+    the benchmark's launch configuration; the oracle checks a sample of
+    sequences one by one (sequences are independent)."""
+    sp = W.sweep_spec(variant)
+    lp = W.layer_params(sp)
+    sm = W.slot_map(sp)
+    ri = W.round_inputs(sp, 0, 0)
+    b = batch_from(sp, lp, ri, sm, max_nodes=sp.max_seq_nodes)
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    g = run_gpu(b, pools)
+    assert g.status == 0
+    ssm_gpu = pools.ssm.cpu().numpy()
+    hist_gpu = pools.conv_hist.cpu().numpy()
+    committed = {int(sm[s]) for s in range(b.S) if b.accepted[s] >= 0}
+    untouched = sorted(set(range(b.P)) - committed)
+    assert np.array_equal(ssm_gpu[untouched], lp.ssm[untouched])
+    assert np.array_equal(hist_gpu[untouched], lp.conv_hist[untouched])
+    for s in (0, 37, 63):
+        sub = W.subset(sp, ri, [s])
+        bs = batch_from(sp, lp, sub, sm[[s]], max_nodes=sp.max_seq_nodes)
+        ref = run_oracle(bs, lp.ssm, lp.conv_hist)
+        n0, n1 = int(ri.node_off[s]), int(ri.node_off[s + 1])
+        assert relerr(g.xc[n0:n1], ref.xc) <= TOL
+        assert np.array_equal(g.win[n0:n1], ref.win)
+        assert relerr(g.o[n0:n1], ref.o) <= TOL
+        assert relerr(g.replay[n0:n1], ref.replay) <= TOL
+        slot = int(sm[s])
+        if b.accepted[s] >= 0:
+            assert relerr(ssm_gpu[slot], ref.ssm[slot]) <= TOL
+        assert np.array_equal(hist_gpu[slot], ref.conv_hist[slot])
+
+
+# ---------------------------------------------------------------- edge cases
+def custom_batch(seed, Hk, Hv, d, sizes, P=None, kind="tree", forest=False, max_nodes=None,
+                 accepted=None):
+    S = len(sizes)
+    P = P or 2 * S + 1
+    sp = W.Spec(f"edge{seed}", W.Shape(S, P, Hk, Hv, d), "tree", list(sizes), seed)
+    lp = W.layer_params(sp)
+    sm = W.slot_map(sp)
+    off = np.zeros(S + 1, np.int32)
+    off[1:] = np.cumsum(sizes)
+    N = int(off[-1])
+    parents = np.empty(N, np.int32)
+    acc = np.empty(S, np.int32)
+    for s, ns in enumerate(sizes):
+        st = W.Stream(seed, 0, W.TID_TREE, 0, s)
+        if kind == "chain":
+            par = [i - 1 for i in range(ns)]
+        else:
+            par = W.random_tree(st, ns, 8 if ns <= 24 else 64, 3)
+        if forest:
+            par = [-1 if (i % 5 == 0) else p for i, p in enumerate(par)]
+        parents[off[s]:off[s + 1]] = par
+        acc[s] = -1 if ns == 0 else int(W.Stream(seed, 0, W.TID_ACC, 0, s).randint(1, ns + 1)[0]) - 1
+    if accepted is not None:
+        acc[:] = accepted
+    C = 2 * Hk * d + Hv * d
+    x = W.Stream(seed, 0, W.TID_X, 0).normal(N * C).reshape(N, C)
+    ba = W.Stream(seed, 0, W.TID_BA, 0).normal(N * 2 * Hv).reshape(N, 2 * Hv)
+    b = Batch(S, P, Hk, Hv, d, max_nodes or (16 if max(sizes) <= 16 else 64), x, ba, parents, off, sm,
+              acc, lp.conv_w, lp.dt_bias, lp.A)
+    return b, lp
+
+
+def run_edge(b, lp, q_scale=1.0, **kw):
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    g = run_gpu(b, pools, q_scale=q_scale, **kw)
+    ref = run_oracle(b, lp.ssm, lp.conv_hist, q_scale=q_scale)
+    compare(g, ref)
+    check_commit(b, pools, ref.ssm, ref.conv_hist, lp.ssm, lp.conv_hist)
+    return g, ref
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("grouped", [True, False])
+def test_widths_and_grouping(d, grouped):
+    Hk, Hv = (2, 4) if grouped else (3, 3)
+    b, lp = custom_batch(100 + d, Hk, Hv, d, [16, 5, 11])
+    run_edge(b, lp)
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_long_sequences_ragged_segments(d):
+    """Trees and chains longer than one 16-node segment, with ragged tails."""
+    b, lp = custom_batch(200 + d, 2, 4, d, [17, 33, 64, 50, 1])
+    run_edge(b, lp)
+    b, lp = custom_batch(300 + d, 2, 2, d, [64, 31], kind="chain")
+    run_edge(b, lp)
+
+
+def test_forest_and_empty_sequences():
+    """Several roots per sequence; empty sequences anywhere in the batch."""
+    b, lp = custom_batch(400, 2, 4, 32, [9, 0, 14, 0, 3], forest=True)
+    run_edge(b, lp)
+
+
+def test_padded_strides_and_q_scale():
+    b, lp = custom_batch(500, 2, 4, 64, [12, 7])
+    run_edge(b, lp, q_scale=0.125, x_pad=12, ba_pad=3, replay_pad=8)
+
+
+def test_small_trees_through_the_multi_segment_kernel():
+    b, lp = custom_batch(600, 2, 4, 128, [16, 3, 9], max_nodes=64)
+    run_edge(b, lp)
+
+
+def test_zero_length_commits_are_identity():
+    b, lp = custom_batch(700, 2, 4, 32, [6, 4, 9], accepted=[-1, -1, -1])
+    run_edge(b, lp)
+
+
+def test_verify_leaves_pools_and_is_deterministic():
+    b, lp = custom_batch(800, 2, 4, 128, [16, 16, 12])
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    g1 = run_gpu(b, pools, commit=False)
+    assert np.array_equal(pools.ssm.cpu().numpy(), lp.ssm)
+    assert np.array_equal(pools.conv_hist.cpu().numpy(), lp.conv_hist)
+    g2 = run_gpu(b, pools, commit=False)
+    for f in ("xc", "win", "o", "replay"):
+        assert np.array_equal(getattr(g1, f), getattr(g2, f)), f
+
+
+def test_verify_alone_on_shared_xc():
+    """Verify parity on identical inputs: both sides get the oracle's xc."""
+    b, lp = custom_batch(900, 2, 4, 128, [16, 9])
+    ref = run_oracle(b, lp.ssm, lp.conv_hist, commit=False)
+    xc32 = ref.xc.astype(np.float32)
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    g = run_gpu(b, pools, commit=False, xc_override=xc32)
+    ref2 = run_oracle(b, lp.ssm, lp.conv_hist, commit=False, xc_override=xc32)
+    compare(g, ref2, check_xc=False)
