@@ -1,0 +1,485 @@
+"""Benchmark of the GDN speculative tree-verify step on one GB300 (or N replicas).
+
+One step = gdn_conv_tree_step + gdn_tree_verify + gdn_commit over one round of
+the throughput sweep: 64 sequences in a 128-slot pool, d = 128, 16-node random
+draft trees (grouped heads H_k = 16, H_v = 32; the headline) plus the other
+three sub-workloads (non-grouped 32/32, 64-token chains).  100 seeded rounds
+are generated on the device before timing; steps cycle through them and the
+pools persist across steps, as in a real decode loop.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is nodes/s over all ranks (each rank a
+replica with its own pools: weak scaling).  L2 is flushed (256 MB write)
+before every timed step; each step is timed with CUDA events on the launching
+stream, per kernel as well.  `e2e` repeats the measurement through the same C
+ABI from pinned host buffers, with the step's inputs copied in and its output
+copied out inside the timed region.  `cpu_baseline` times the oracle on the
+host cores on a bounded sample of the same workload.  `--impl reference` times
+the oracle alone (the only reference implementation of this method here).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gdn_workloads as W  # noqa: E402
+
+METRIC = "GDN tree-verify+commit nodes/s and achieved HBM GB/s (% of GB300 peak)"
+HEADLINE = "grouped_tree16"
+N_ROUNDS = 100
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ algorithmic bytes
+def algo_bytes(sp: W.Spec, parents: np.ndarray, node_off: np.ndarray, accepted: np.ndarray):
+    """Bytes the method must move per launch (conv weights once per layer)."""
+    sh = sp.shape
+    S, Hv, d = sh.n_seqs, sh.h_v, sh.d
+    C = sh.conv_channels
+    N = int(node_off[-1])
+    conv = N * C * 4 + S * 3 * C * 4 + 16 * C + N * C * 4 + N * 3 * C * 4
+    verify = S * Hv * d * d * 4 + N * C * 4 + N * 2 * Hv * 4 + N * Hv * d * 4 + N * Hv * (2 * d + 1) * 4
+    commit = 0
+    for s in range(S):
+        a = int(accepted[s])
+        if a < 0:
+            continue
+        n0 = int(node_off[s])
+        m = 0
+        while a >= 0:
+            m += 1
+            a = int(parents[n0 + a])
+        commit += 2 * Hv * d * d * 4 + m * Hv * (2 * d + 1) * 4 + 2 * 3 * C * 4
+    return {"conv": conv, "verify": verify, "commit": commit}
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workload
+class DeviceWorkload:
+    """Pools, weights and N_ROUNDS rounds of inputs resident on the device.
+
+    Tree structure, accepted nodes, gate projections and conv weights come from
+    the SplitMix64 generator of gdn_workloads; the bulk tensors (tokens x and
+    the two pools) are drawn on the device with torch's Philox generator keyed
+    by the same stream keys, with the same distributions."""
+
+    def __init__(self, sp: W.Spec, rounds: int, device, seed_offset: int = 0):
+        import torch
+        self.sp, self.device = sp, device
+        sh = sp.shape
+        self.C = sh.conv_channels
+        self.rs = (2 * sh.d + 1 + 3) // 4 * 4           # smallest replay row stride
+        lp = W.layer_params(sp, 0, with_pools=False)
+        g = torch.Generator(device=device)
+        g.manual_seed(W.stream_key(sp.seed, seed_offset, W.TID_STATE) & ((1 << 63) - 1))
+        self.ssm = torch.randn((sh.n_slots, sh.h_v, sh.d, sh.d), generator=g, device=device) * 0.1
+        g.manual_seed(W.stream_key(sp.seed, seed_offset, W.TID_HIST) & ((1 << 63) - 1))
+        self.hist = torch.randn((sh.n_slots, 3, self.C), generator=g, device=device)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.w, self.dt, self.A = t(lp.conv_w), t(lp.dt_bias), t(lp.A)
+        self.slot_map = t(W.slot_map(sp))
+        self.rounds = []
+        self.host_rounds = []
+        for r in range(rounds):
+            ri = W.round_inputs(sp, 0, r, with_x=False)
+            g.manual_seed(W.stream_key(sp.seed, seed_offset, W.TID_X, r) & ((1 << 63) - 1))
+            x = torch.randn((int(ri.node_off[-1]), self.C), generator=g, device=device)
+            self.rounds.append(dict(x=x, ba=t(ri.ba), parents=t(ri.parents), node_off=t(ri.node_off),
+                                    accepted=t(ri.accepted)))
+            self.host_rounds.append(ri)
+        N = int(self.host_rounds[0].node_off[-1])
+        self.N = N
+        self.xc = torch.empty((N, self.C), device=device)
+        self.win = torch.empty((N, 3, self.C), device=device)
+        self.o = torch.empty((N, sh.h_v, sh.d), device=device)
+        self.replay = torch.empty((N, sh.h_v, self.rs), device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        import gated_deltanet_speculative_gdn_gb300 as G
+        self.G = G
+        self.dims = G.GdnDims.make(sh.n_seqs, N, sh.n_slots, sh.h_k, sh.h_v, sh.d, sp.max_seq_nodes)
+
+    def step(self, r, events=None, inputs=None):
+        """conv -> verify -> commit on round r; events[i] recorded before call i."""
+        G, sh = self.G, self.sp.shape
+        R = inputs if inputs is not None else self.rounds[r]
+        if events:
+            events[0].record()
+        G.gdn_conv_tree_step(self.dims, R["x"], self.C, self.w, self.hist, R["parents"], R["node_off"],
+                             self.slot_map, self.xc, self.win, self.status)
+        if events:
+            events[1].record()
+        G.gdn_tree_verify(self.dims, self.xc, R["ba"], 2 * sh.h_v, self.dt, self.A, self.ssm, 1.0,
+                          R["parents"], R["node_off"], self.slot_map, self.o, self.replay, self.rs,
+                          self.status)
+        if events:
+            events[2].record()
+        G.gdn_commit(self.dims, R["accepted"], R["parents"], R["node_off"], self.slot_map, self.replay,
+                     self.rs, self.win, self.ssm, self.hist, self.status)
+        if events:
+            events[3].record()
+
+
+def source_sha(name: str) -> str:
+    p = os.path.join(ROOT, "gated_deltanet_speculative_gdn_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+KERNEL_SRC = {"conv": "gdn_conv.cu", "verify": "gdn_verify.cu", "commit": "gdn_commit.cu"}
+
+
+def ncu_traffic(kernel: str, variant: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None
+    when absent or when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f)
+        e = t[variant][kernel]
+        if e.get("src_sha") != source_sha(KERNEL_SRC[kernel]):
+            return None
+        return int(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int = 0,
+                 e2e: bool = False, clocks: bool = False):
+    import torch
+    sp = W.sweep_spec(variant, rounds=N_ROUNDS)
+    wl = DeviceWorkload(sp, min(N_ROUNDS, max(steps + warmup, 1)), device, seed_offset)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    nr = len(wl.rounds)
+    for i in range(warmup):
+        flush.fill_(float(i))
+        wl.step(i % nr)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if clocks else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(float(i))                        # L2 flush, outside the step's events
+        wl.step((warmup + i) % nr, ev[i])
+        ends[i].record()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__exit__()
+    assert int(wl.status.item()) == 0, wl.G.gdn_status_str(int(wl.status.item()))
+    per = {"conv": [], "verify": [], "commit": []}
+    step_ms = []
+    for i in range(steps):
+        e = ev[i] + [ends[i]]
+        per["conv"].append(e[0].elapsed_time(e[1]))
+        per["verify"].append(e[1].elapsed_time(e[2]))
+        per["commit"].append(e[2].elapsed_time(e[3]))
+        step_ms.append(e[0].elapsed_time(e[3]))
+    bytes_ = [algo_bytes(sp, wl.host_rounds[(warmup + i) % nr].parents, wl.host_rounds[(warmup + i) % nr].node_off,
+                         wl.host_rounds[(warmup + i) % nr].accepted) for i in range(steps)]
+    out = {"sp": sp, "wl": wl, "step_ms": step_ms, "per": per, "bytes": bytes_,
+           "clocks": sampler.summary() if sampler else None}
+    if e2e:
+        out["e2e"] = time_e2e(wl, steps, warmup)
+    return out
+
+
+def time_e2e(wl: DeviceWorkload, steps: int, warmup: int, host_rounds: int = 8):
+    """Same step through the C ABI from pinned host buffers: H2D of the step's
+    inputs and D2H of its attention output inside the timed region."""
+    import torch
+    nr = min(host_rounds, len(wl.rounds))
+    host = []
+    for r in range(nr):
+        host.append({k: v.cpu().pin_memory() for k, v in wl.rounds[r].items()})
+    dev_in = {k: torch.empty_like(v) for k, v in wl.rounds[0].items()}
+    o_host = torch.empty(wl.o.shape, dtype=wl.o.dtype).pin_memory()
+    st_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = wl.o.numel() * wl.o.element_size() + 4
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=wl.device)
+
+    def one(r):
+        for k, v in host[r].items():
+            dev_in[k].copy_(v, non_blocking=True)
+        wl.step(r, None, dev_in)
+        o_host.copy_(wl.o, non_blocking=True)
+        st_host.copy_(wl.status, non_blocking=True)
+
+    for i in range(warmup):
+        one(i % nr)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        one((warmup + i) % nr)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    return {"ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# -------------------------------------------------------------- CPU baseline
+def oracle_sample(variant: str, budget_s: float = 12.0, seqs_per_step=None):
+    """Times the oracle (single-threaded C) on whole sequences of the sweep
+    workload until the budget is spent.  Returns (nodes, seconds, sequences)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle as O
+    orc = O.get()
+    sp = W.sweep_spec(variant)
+    sh = sp.shape
+    lp = W.layer_params(sp, 0, with_pools=False)
+    nodes, secs, done = 0, 0.0, 0
+    ri = W.round_inputs(sp, 0, 0)
+    s = 0
+    while True:
+        sub = W.subset(sp, ri, [s % sh.n_seqs])
+        n = int(sub.node_off[-1])
+        # a one-slot pool holding this sequence's state and history
+        ssm = W.Stream(sp.seed, 1000 + s, W.TID_STATE).normal(sh.h_v * sh.d * sh.d, 0.1).reshape(
+            1, sh.h_v, sh.d, sh.d)
+        hist = W.Stream(sp.seed, 1000 + s, W.TID_HIST).normal(3 * sh.conv_channels).reshape(1, 3, -1)
+        dm = O.Dims(1, n, 1, sh.h_k, sh.h_v, sh.d)
+        t0 = time.perf_counter()
+        rc, xc, win = orc.conv_tree_step(dm, sub.x, lp.conv_w, hist, sub.parents, sub.node_off, [0])
+        rc2, o, rep = orc.tree_verify(dm, xc.astype(np.float32), sub.ba, lp.dt_bias, lp.A, ssm,
+                                      sub.parents, sub.node_off, [0])
+        rc3 = orc.commit(dm, sub.accepted, sub.parents, sub.node_off, [0], rep, win, ssm, hist)
+        secs += time.perf_counter() - t0
+        assert rc == rc2 == rc3 == 0
+        nodes += n
+        done += 1
+        s += 1
+        if (seqs_per_step is not None and done >= seqs_per_step) or (seqs_per_step is None and secs >= budget_s):
+            break
+    return nodes, secs, done
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variants", default="all", help="'all' or a comma list of sweep variants")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    peak, peak_kind = measured_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return reference_arm(args, peak, peak_kind)
+
+    import torch
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    variants = list(W.SWEEP_VARIANTS) if args.variants == "all" else args.variants.split(",")
+    if HEADLINE in variants:
+        variants.remove(HEADLINE)
+    head = time_variant(HEADLINE, args.steps, args.warmup, device, seed_offset=rank, e2e=True, clocks=True)
+    others = {v: time_variant(v, args.steps, args.warmup, device, seed_offset=rank) for v in variants}
+
+    sp = head["sp"]
+    N = head["wl"].N
+    step_ms = statistics.mean(head["step_ms"])
+    e2e_ms = head["e2e"]["ms_per_step"]
+    if dist is not None:
+        t = torch.tensor([step_ms, e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+        dist.barrier()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    nodes_total = N * world
+    value = nodes_total / (step_ms * 1e-3)
+    kern_ms = {k: statistics.mean(v) for k, v in head["per"].items()}
+    kb = {k: statistics.mean(b[k] for b in head["bytes"]) for k in ("conv", "verify", "commit")}
+    step_bytes = sum(kb.values())
+    dom = max(kern_ms, key=kern_ms.get)
+    achieved = kb[dom] / (kern_ms[dom] * 1e-3) / 1e9
+    traffic = ncu_traffic(dom, HEADLINE)
+    kernels = {k: {"ms": round(kern_ms[k], 5), "algo_bytes": int(kb[k]),
+                   "gbs": round(kb[k] / (kern_ms[k] * 1e-3) / 1e9, 1),
+                   "frac": round(kb[k] / (kern_ms[k] * 1e-3) / 1e9 / peak, 4),
+                   "share": round(kern_ms[k] / sum(kern_ms.values()), 4)} for k in kern_ms}
+    sweep = {}
+    for v, r in others.items():
+        ms = statistics.mean(r["step_ms"])
+        b = statistics.mean(sum(x.values()) for x in r["bytes"])
+        sweep[v] = {"nodes_per_s": round(r["wl"].N / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
+                    "step_gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                    "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                    "kernels_ms": {k: round(statistics.mean(x), 5) for k, x in r["per"].items()}}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        nodes, secs, nseq = oracle_sample(HEADLINE)
+        cpu = {"value": round(nodes / secs, 2), "unit": "nodes/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nseq} of 64 sequences ({nodes} nodes) of the {HEADLINE} workload, "
+                         f"conv+verify+commit, {secs:.1f} s single-threaded C"}
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "nodes/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 structure, Philox bulk tensors)",
+        "config": {"workload": f"sweep_{HEADLINE}: 64 seqs x 16-node trees, 128-slot pool, H_k=16, "
+                               f"H_v=32, d=128, d_conv=4, one layer, {N_ROUNDS} rounds",
+                   "n_seqs": 64, "nodes_per_step": N, "h_k": 16, "h_v": 32, "d": 128,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step (256 MB write)"},
+        "hbm": {"step_algo_bytes": int(step_bytes),
+                "step_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
+                "frac_of_peak": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+                "peak_gbs": peak, "peak_kind": peak_kind},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": peak_kind},
+        "kernels": kernels,
+        "sweep": sweep,
+        "e2e": {"value": round(nodes_total / (e2e_ms * 1e-3), 1), "unit": "nodes/s",
+                "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": head["e2e"]["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": head["e2e"]["d2h_bytes_per_step"]},
+        "gpu_launches": 4 * args.steps * (1 + len(others)),
+        "clocks": head["clocks"],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def reference_arm(args, peak, peak_kind):
+    """The oracle, as it stands, on the host cores; each step a bounded sample
+    (two whole sequences) of the headline workload."""
+    for _ in range(args.warmup):
+        oracle_sample(HEADLINE, seqs_per_step=1)
+    nodes, secs = 0, 0.0
+    for _ in range(args.steps):
+        n, t, _ = oracle_sample(HEADLINE, seqs_per_step=2)
+        nodes += n
+        secs += t
+    value = nodes / secs
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "nodes/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"sweep_{HEADLINE} (2 of 64 sequences per step)"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "nodes/s", "cores": 1, "kind": "oracle",
+                         "sample": f"2 sequences (32 nodes) per step, {args.steps} steps"},
+        "e2e": {"value": round(value, 2), "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
