@@ -392,6 +392,332 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
     }
 }
 
+// ============================================================================
+// Tensor-core variant for d = 128 and trees of at most 16 nodes.
+//
+// The contraction D[i][c] = sum_k S0[i][k] B[c][k], with B = [k^_0..k^_15 |
+// q^_0..q^_15] (unscaled), is a 128 x 32 x 128 matrix product per (sequence,
+// head).  It runs on tcgen05 with the accumulators in tensor memory, in three
+// tf32 products that recover fp32 accuracy (x = hi + lo, hi = x with the low
+// 13 mantissa bits cleared, lo exact):
+//     D = A_hi B_hi + A_hi B_lo + A_lo B_hi      (the dropped A_lo B_lo ~ 2^-22)
+// The tensor cores align and truncate when they accumulate, so the large
+// A_hi B_hi term of each K-chunk gets an accumulator of its own and the two
+// small terms share one more; the epilogue adds them in fp32.
+// S0 streams through a two-slot ring of 16 KB K-chunks ([128 rows][32 floats],
+// TMA, 128-byte swizzle, which is also the tensor cores' K-major operand
+// layout); the CTA splits each chunk into hi (in place) and lo, one thread
+// issues the chunk's 12 MMAs, and the chunk after next is loaded into the slot
+// once the MMAs that read it have completed.  The path coefficients need only
+// the dot products along each node's ancestor path: each warp holds the k^ and
+// q^ of its four nodes in registers and forms them with shuffle reductions.
+// Gamma_t scales column t in the epilogue, where thread i reads row i of the
+// accumulators straight from tensor memory.  ~100 KB of shared memory: two
+// CTAs per SM.
+namespace tcv {
+constexpr int D = 128;
+constexpr uint32_t kChunk = 128 * 128;        // bytes of one S0 K-chunk
+constexpr uint32_t kBChunk = 32 * 128;        // bytes of one B K-chunk
+constexpr uint32_t RAW = 0;                   // 2 slots: S0 chunk, hi in place
+constexpr uint32_t LO = RAW + 2 * kChunk;     // 2 slots: lo of the chunk
+constexpr uint32_t BHI = LO + 2 * kChunk;     // B hi, 4 K-chunks
+constexpr uint32_t BLO = BHI + 4 * kBChunk;   // B lo
+constexpr uint32_t SMALL = BLO + 4 * kBChunk;
+// float offsets inside the small area
+constexpr int CK = 0, CQ = CK + 256, BETA = CQ + 256, DEC = BETA + 16, GAM = DEC + 16, PAR = GAM + 16,
+              BARS = PAR + 16, TMEMA = BARS + 8, SMALL_FLOATS = TMEMA + 4;
+constexpr size_t BYTES = SMALL + SMALL_FLOATS * 4 + 1024;
+// instruction descriptor: D fp32, A and B tf32, both K-major, M = 128, N = 32
+constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+// columns 32 kb: A_hi B_hi of K-chunk kb; columns 128..159: the two small terms
+constexpr uint32_t TMEM_COLS = 256, SMALL_COL = 128;
+
+// byte offset of element k of row `row` in a [rows][32 floats]-per-chunk,
+// 128-byte-swizzled, K-major buffer (chunk size `chunk` bytes)
+__device__ __forceinline__ uint32_t sw_off(int row, int k, uint32_t chunk) {
+    return uint32_t(k >> 5) * chunk + uint32_t(row) * 128u + ((uint32_t(((k & 31) >> 2) ^ (row & 7))) << 4) +
+           uint32_t(k & 3) * 4u;
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+}  // namespace tcv
+
+__global__ void __launch_bounds__(kThreads, 2)
+    tree_verify_tc_kernel(const __grid_constant__ CUtensorMap tmap, const VerifyArgs a) {
+    using namespace tcv;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sb =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = gdn::smem_addr(sb);
+    float *small = reinterpret_cast<float *>(sb + SMALL);
+    float *cks = small + CK, *cqs = small + CQ;
+    float *beta_s = small + BETA, *dec_s = small + DEC, *gam_s = small + GAM;
+    int *par = reinterpret_cast<int *>(small + PAR);
+    uint64_t *full = reinterpret_cast<uint64_t *>(small + BARS);  // [2] chunk landed
+    uint64_t *mmab = full + 2;                                     // [2] chunk's MMAs done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + TMEMA);
+    __shared__ int hdr[4];  // error, first node, node count, slot
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int kh = h / (a.Hv / a.Hk);
+
+    if (tid == 0) {
+        const int n0 = a.node_off[s], n1 = a.node_off[s + 1];
+        int err = 0;
+        if (n0 < 0 || n1 < n0 || n1 > a.N || (s == 0 && n0 != 0) || (s == a.S - 1 && n1 != a.N) ||
+            n1 - n0 > a.max_nodes || n1 - n0 > kSeg)
+            err = GDN_DEV_BAD_NODE_OFF;
+        const int slot = a.slot_map[s];
+        if (!err && (slot < 0 || slot >= a.P)) err = GDN_DEV_BAD_SLOT;
+        hdr[0] = err;
+        hdr[1] = n0;
+        hdr[2] = n1 - n0;
+        hdr[3] = slot;
+    }
+    __syncthreads();
+    if (hdr[0] || hdr[2] == 0) {
+        if (tid == 0 && hdr[0]) gdn::record_status(a.status, hdr[0]);
+        return;
+    }
+    const int n0 = hdr[1], lc = hdr[2], slot = hdr[3];
+    if (tid < lc) {
+        const int p = a.parents[n0 + tid];
+        par[tid] = p;
+        if (p < -1 || p >= tid) hdr[0] = GDN_DEV_BAD_PARENT;
+    }
+    __syncthreads();
+    if (hdr[0]) {
+        if (tid == 0) gdn::record_status(a.status, hdr[0]);
+        return;
+    }
+    // ---- set-up: barriers, tensor memory, first two S0 chunks ---------------
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) gdn::mbar_init(full + i, 1);
+        gdn::fence_mbar_init();
+    }
+    if (warp == 0) {
+        gdn::tmem_alloc(tmem_slot, TMEM_COLS);
+        gdn::tmem_relinquish();
+    }
+    gdn::tc_fence_before_sync();
+    __syncthreads();
+    gdn::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int ybox = (slot * a.Hv + h) * D;
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            gdn::mbar_arrive_expect_tx(full + b, kChunk);
+            gdn::tma_load_2d(sb + RAW + b * kChunk, &tmap, 32 * b, ybox, full + b);
+        }
+    }
+
+    // ---- A: v of this row, gates, normalised q and k into B (hi / lo) --------
+    const int64_t C = a.C;
+    const int qoff = kh * D, koff = a.Hk * D + kh * D, voff = 2 * a.Hk * D + h * D;
+    float vreg[kSeg];
+#pragma unroll
+    for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? __ldg(a.xc + (n0 + t) * C + voff + tid) : 0.0f;
+    if (warp == 0 && lane < lc) {
+        const int64_t n = n0 + lane;
+        const float bv = __ldg(a.ba + n * a.ba_stride + h);
+        const float av = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
+        const float dec = expf(gdn::softplus_f(av + a.dt_bias[h]) * a.A[h]);
+        beta_s[lane] = gdn::sigmoid_f(bv);
+        dec_s[lane] = dec;
+        a.replay[(n * a.Hv + h) * a.rstride + 2 * D] = dec;
+    }
+    // warp w normalises B rows c = w + 4 j: k^ of nodes w, w+4, w+8, w+12
+    // (j < 4) and q^ of the same nodes (j >= 4); lane l holds elements 4l..4l+3
+    float4 nv[8];
+    {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = warp + 4 * j, t = c & 15;
+            nv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < lc)
+                nv[j] = __ldg(reinterpret_cast<const float4 *>(a.xc + (n0 + t) * C + (c < kSeg ? koff : qoff) +
+                                                               4 * lane));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = warp + 4 * j, t = c & 15;
+            float ss = nv[j].x * nv[j].x;
+            ss = fmaf(nv[j].y, nv[j].y, ss);
+            ss = fmaf(nv[j].z, nv[j].z, ss);
+            ss = fmaf(nv[j].w, nv[j].w, ss);
+            ss = gdn::warp_sum(ss);
+            nv[j] = scale4(nv[j], rsqrtf(ss + 1e-6f));
+            const float4 hi = make_float4(gdn::tf32_hi(nv[j].x), gdn::tf32_hi(nv[j].y), gdn::tf32_hi(nv[j].z),
+                                          gdn::tf32_hi(nv[j].w));
+            const float4 lo = make_float4(nv[j].x - hi.x, nv[j].y - hi.y, nv[j].z - hi.z, nv[j].w - hi.w);
+            const uint32_t off = sw_off(c, 4 * lane, kBChunk);
+            *reinterpret_cast<float4 *>(sb + BHI + off) = hi;
+            *reinterpret_cast<float4 *>(sb + BLO + off) = lo;
+            if (c < kSeg && t < lc)
+                *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride + 4 * lane) =
+                    nv[j];
+        }
+    }
+    gdn::fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- C: path coefficients and Gamma; warp w handles its own four nodes ---
+    // For node t and each ancestor j (walking up), with gamma = the decays
+    // strictly after j up to t:  cks[t][j] = gamma k^_j . k^_t,
+    // cqs[t][j] = gamma k^_j . q^_t;  cqs[t][t] = k^_t . q^_t;  Gamma_t = all decays.
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const int t = warp + 4 * jj;
+        if (t < lc) {
+            const float4 kt = nv[jj], qt = nv[4 + jj];
+            float ck = 0.f, cq = 0.f;  // lane j < 16 owns entry j of row t
+            const float self = gdn::warp_sum(gdn::fma4(kt, qt, 0.f));
+            if (lane == t) cq = self;
+            float gam = dec_s[t];
+            for (int j = par[t]; j >= 0; j = par[j]) {
+                const uint32_t oj = sw_off(j, 4 * lane, kBChunk);
+                const float4 kj = add4(*reinterpret_cast<const float4 *>(sb + BHI + oj),
+                                       *reinterpret_cast<const float4 *>(sb + BLO + oj));
+                const float kk = gdn::warp_sum(gdn::fma4(kj, kt, 0.f));
+                const float kq = gdn::warp_sum(gdn::fma4(kj, qt, 0.f));
+                if (lane == j) {
+                    ck = gam * kk;
+                    cq = gam * kq;
+                }
+                gam *= dec_s[j];
+            }
+            if (lane < kSeg) {
+                cks[t * kSeg + lane] = ck;
+                cqs[t * kSeg + lane] = cq;
+            }
+            if (lane == 0) gam_s[t] = gam;
+        }
+    }
+
+    // ---- D: S0 chunks through the ring, 3 x tf32 MMAs per K-step -------------
+    bool ok = true;
+    for (int kb = 0; kb < 4; ++kb) {
+        const int sl = kb & 1;
+        if (!gdn::mbar_wait_bounded(full + sl, uint32_t(kb >> 1))) hdr[0] = GDN_DEV_TIMEOUT;
+        float4 *raw = reinterpret_cast<float4 *>(sb + RAW + sl * kChunk);
+        float4 *lo = reinterpret_cast<float4 *>(sb + LO + sl * kChunk);
+#pragma unroll
+        for (int j = 0; j < int(kChunk / 16 / kThreads); ++j) {
+            const int f = tid + kThreads * j;
+            const float4 x = raw[f];
+            const float4 hi = make_float4(gdn::tf32_hi(x.x), gdn::tf32_hi(x.y), gdn::tf32_hi(x.z),
+                                          gdn::tf32_hi(x.w));
+            raw[f] = hi;
+            lo[f] = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+        }
+        gdn::fence_proxy_async_smem();
+        __syncthreads();
+        if (hdr[0]) {
+            ok = false;
+            break;
+        }
+        if (tid == 0) {
+            gdn::tc_fence_after_sync();
+            const uint32_t dbig = tmem + 32u * kb;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ahi = gdn::desc_sw128(sbase + RAW + sl * kChunk + ks * 32);
+                const uint64_t alo = gdn::desc_sw128(sbase + LO + sl * kChunk + ks * 32);
+                const uint64_t bhi = gdn::desc_sw128(sbase + BHI + kb * kBChunk + ks * 32);
+                const uint64_t blo = gdn::desc_sw128(sbase + BLO + kb * kBChunk + ks * 32);
+                gdn::mma_tf32(dbig, ahi, bhi, IDESC, ks != 0);
+                gdn::mma_tf32(tmem + SMALL_COL, ahi, blo, IDESC, (kb | ks) != 0);
+                gdn::mma_tf32(tmem + SMALL_COL, alo, bhi, IDESC, 1);
+            }
+            gdn::mma_commit(mmab + sl);
+            if (kb < 2) {
+                // the slot is free once the MMAs reading it have completed
+                if (gdn::mbar_wait_bounded(mmab + sl, 0)) {
+                    gdn::mbar_arrive_expect_tx(full + sl, kChunk);
+                    gdn::tma_load_2d(sb + RAW + sl * kChunk, &tmap, 32 * (kb + 2), ybox, full + sl);
+                } else {
+                    hdr[0] = GDN_DEV_TIMEOUT;
+                }
+            }
+        }
+    }
+
+    if (ok) {
+        // the last commit covers every MMA of the CTA
+        if (!gdn::mbar_wait_bounded(mmab + 1, 1)) hdr[0] = GDN_DEV_TIMEOUT;
+        __syncthreads();
+        ok = hdr[0] == 0;
+    }
+    if (ok) {
+        gdn::tc_fence_after_sync();
+        const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+        float dv[32];
+        {
+            float p1[32];
+            gdn::tmem_ld32(trow + 0, dv);
+            gdn::tmem_ld32(trow + 32, p1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+            float p2[32];
+            gdn::tmem_ld32(trow + 64, p1);
+            gdn::tmem_ld32(trow + 96, p2);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dv[i] += p1[i] + p2[i];
+            gdn::tmem_ld32(trow + SMALL_COL, p1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+        }
+
+        // ---- E: per row, the nodes in order ----------------------------------
+        float u[kSeg];
+#pragma unroll
+        for (int t = 0; t < kSeg; ++t) {
+            u[t] = 0.f;
+            if (t < lc) {
+                const int64_t n = n0 + t;
+                float sk = gam_s[t] * dv[t];
+                float oq = gam_s[t] * dv[kSeg + t];
+#pragma unroll
+                for (int j4 = 0; j4 < (t + 4) / 4; ++j4) {
+                    const float4 ckv = *reinterpret_cast<const float4 *>(cks + t * kSeg + 4 * j4);
+                    const float4 cqv = *reinterpret_cast<const float4 *>(cqs + t * kSeg + 4 * j4);
+                    if (4 * j4 + 0 < t) sk = fmaf(ckv.x, u[4 * j4 + 0], sk);
+                    if (4 * j4 + 1 < t) sk = fmaf(ckv.y, u[4 * j4 + 1], sk);
+                    if (4 * j4 + 2 < t) sk = fmaf(ckv.z, u[4 * j4 + 2], sk);
+                    if (4 * j4 + 3 < t) sk = fmaf(ckv.w, u[4 * j4 + 3], sk);
+                    if (4 * j4 + 0 < t) oq = fmaf(cqv.x, u[4 * j4 + 0], oq);
+                    if (4 * j4 + 1 < t) oq = fmaf(cqv.y, u[4 * j4 + 1], oq);
+                    if (4 * j4 + 2 < t) oq = fmaf(cqv.z, u[4 * j4 + 2], oq);
+                    if (4 * j4 + 3 < t) oq = fmaf(cqv.w, u[4 * j4 + 3], oq);
+                }
+                u[t] = beta_s[t] * (vreg[t] - sk);
+                oq = fmaf(cqs[t * kSeg + t], u[t], oq);
+                a.o[(n * a.Hv + h) * D + tid] = a.q_scale * oq;
+                a.replay[(n * a.Hv + h) * a.rstride + D + tid] = u[t];
+            }
+        }
+    } else {
+        // a wait ran out: drain what may still be in flight (bounded) before
+        // the shared and tensor memory are released
+        if (tid == 0) {
+            gdn::record_status(a.status, GDN_DEV_TIMEOUT);
+            gdn::mbar_wait_bounded(full + 0, 0);
+            gdn::mbar_wait_bounded(full + 1, 0);
+            gdn::mbar_wait_bounded(mmab + 0, 0);
+            gdn::mbar_wait_bounded(mmab + 1, 0);
+        }
+    }
+    gdn::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        gdn::tc_fence_after_sync();
+        gdn::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *p = nullptr;
@@ -432,9 +758,24 @@ int launch(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
+int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
+    auto k = tree_verify_tc_kernel;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tcv::BYTES)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    const dim3 grid{unsigned(a.Hv), unsigned(a.S)};
+    k<<<grid, kThreads, tcv::BYTES, st>>>(map, a);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+// d = 128 with trees of up to 16 nodes: tensor cores; otherwise the FFMA kernel
 template <int D>
 int launch_d(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
-    return a.max_nodes <= kSeg ? launch<D, kSeg>(map, a, st) : launch<D, gdn::kMaxSeqNodes>(map, a, st);
+    if constexpr (D == 128) {
+        if (a.max_nodes <= kSeg) return launch_tc(map, a, st);
+        return launch<D, gdn::kMaxSeqNodes>(map, a, st);
+    } else {
+        return a.max_nodes <= kSeg ? launch<D, kSeg>(map, a, st) : launch<D, gdn::kMaxSeqNodes>(map, a, st);
+    }
 }
 
 }  // namespace
