@@ -14,21 +14,19 @@
 //  preflight  one warp per sequence: node range, accepted node, the parent walk
 //             (parents held in two registers per lane, walked by shuffles) and
 //             slot uniqueness among committing sequences.  Writes *status.
-//  apply      one CTA per (value head, sequence); does nothing unless *status
-//             is zero.  The path's replay rows are applied in closed form
+//  apply      CTAs of 32 state rows of one (value head, sequence); do nothing
+//             unless *status is zero.  The path's replay rows are applied in
+//             closed form
 //                 S = Gamma S0 + sum_j c_j u_j k_j^T,   c_j = prod of decays after j
 //             which equals applying S <- decay_j S + u_j k_j^T root first.  The
-//             state tile is held in registers (coalesced 128-bit loads and
-//             stores), the replay rows are staged in shared memory 16 at a time.
-//             The CTA also copies its share of the accepted node's window into
-//             the slot's conv history.
+//             state rows are held in registers (coalesced 128-bit loads and
+//             stores); each warp also copies its share of the accepted node's
+//             window into the slot's conv history.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
 namespace {
 
-constexpr int kApplyThreads = 256;
-constexpr int kStage = 16;  // replay rows staged per pass
 
 struct CommitArgs {
     const int32_t *__restrict__ accepted;
@@ -77,114 +75,130 @@ __global__ void __launch_bounds__(256) commit_preflight_kernel(const CommitArgs 
     if (err && lane == 0) gdn::record_status(a.status, err);
 }
 
+// Apply: every warp works alone, with no block barrier.  A CTA of four warps
+// covers 32 state rows of one (head, sequence); warp w owns 8 of them (lane l:
+// row group l / (d/4), float4 column group l % (d/4)).  The warp reads the
+// sequence header, issues the loads of its rows at once, walks the accepted
+// path with register shuffles (parents two per lane), forms the closed-form
+// coefficients with a warp scan of the path's decays, and applies the path's
+// rank-one terms from the replay rows (shared by the CTAs of the head: L1/L2
+// hits), the next step's rows loading while the current one is applied.
+constexpr int kWarpRows = 8;                      // state rows per warp
+constexpr int kApplyWarps = 4;
+constexpr int kCtaRows = kWarpRows * kApplyWarps; // state rows per CTA
+
 template <int D>
-__global__ void __launch_bounds__(kApplyThreads) commit_apply_kernel(const CommitArgs a) {
-    constexpr int DV4 = D / 4;
-    constexpr int GROUPS = kApplyThreads / DV4;              // row groups
-    constexpr int RPT = D / GROUPS > 0 ? D / GROUPS : 1;     // rows per thread
-    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
-    __shared__ int hdr[4];  // go, first node, path length, slot
-    __shared__ int par[gdn::kMaxSeqNodes];
-    __shared__ int path[gdn::kMaxSeqNodes];   // root first
-    __shared__ float coef[gdn::kMaxSeqNodes];
-    __shared__ float gam_s;
-    __shared__ __align__(16) float kst[kStage][D];
-    __shared__ __align__(16) float ust[kStage][D];
+__global__ void __launch_bounds__(kApplyWarps * 32) commit_apply_warp_kernel(const CommitArgs a) {
+    constexpr int DV4 = D / 4;               // float4 chunks per row (<= 32)
+    constexpr int RI = 32 / DV4;             // rows one warp instruction covers
+    constexpr int NF = kWarpRows / RI;       // float4 per lane
+    constexpr int CPH = (D + kCtaRows - 1) / kCtaRows;  // CTAs per head
+    static_assert(NF >= 1, "d >= 16");
+    const int hq = blockIdx.x, s = blockIdx.y;
+    const int h = hq / CPH, q = hq % CPH;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned full = 0xffffffffu;
+    const int rbase = q * kCtaRows + warp * kWarpRows;  // first row of the warp
 
-    if (tid == 0) {
-        const int st = *reinterpret_cast<volatile int32_t *>(a.status);
-        const int acc = a.accepted[s];
-        hdr[0] = (st == 0 && acc >= 0);
-        hdr[1] = a.node_off[s];
-        hdr[2] = acc;  // accepted node for now
-        hdr[3] = a.slot_map[s];
-    }
-    __syncthreads();
-    if (!hdr[0]) return;
-    const int n0 = hdr[1], acc = hdr[2], slot = hdr[3];
-    // the preflight has checked the walk; load the parents up to the accepted node
-    for (int i = tid; i <= acc; i += kApplyThreads) par[i] = a.parents[n0 + i];
-    __syncthreads();
-    if (tid == 0) {
-        int m = 0;
-        for (int cur = acc; cur >= 0; cur = par[cur]) ++m;
-        int k = m;
-        for (int cur = acc; cur >= 0; cur = par[cur]) path[--k] = cur;
-        hdr[2] = m;
-    }
-    __syncthreads();
-    const int m = hdr[2];
-    // decays of the path, then the closed-form coefficients (serial product)
-    for (int i = tid; i < m; i += kApplyThreads)
-        coef[i] = __ldg(a.replay + ((int64_t(n0) + path[i]) * a.Hv + h) * a.rstride + 2 * D);
-    __syncthreads();
-    if (tid == 0) {
-        float g = 1.0f;
-        for (int i = m - 1; i >= 0; --i) {
-            const float dec = coef[i];
-            coef[i] = g;
-            g *= dec;
-        }
-        gam_s = g;
-    }
+    // the preflight (earlier on this stream) has checked every index; the range
+    // tests here only keep the loads below in bounds
+    const int st = *reinterpret_cast<volatile int32_t *>(a.status);
+    const int acc = a.accepted[s], n0 = a.node_off[s], n1 = a.node_off[s + 1], slot = a.slot_map[s];
+    if (!(st == 0 && acc >= 0 && n0 >= 0 && n1 <= a.N && acc < n1 - n0 && acc < gdn::kMaxSeqNodes && slot >= 0 &&
+          slot < a.P))
+        return;
 
-    // state tile: thread owns float4 column group kc of rows rg + GROUPS * r
-    const int kc = tid % DV4, rg = tid / DV4;
-    const bool active = rg < D;  // D = 16 leaves some threads idle
+    {
+        // this warp's share of the window copy: conv_hist[slot] <- win[accepted]
+        const int64_t total4 = int64_t(3) * a.C / 4;
+        const int64_t parts = int64_t(a.Hv) * CPH * kApplyWarps;
+        const int64_t per = (total4 + parts - 1) / parts;
+        const int64_t lo = ((int64_t(h) * CPH + q) * kApplyWarps + warp) * per, hi = min(total4, lo + per);
+        const float4 *wsrc = reinterpret_cast<const float4 *>(a.win + (int64_t(n0) + acc) * 3 * a.C);
+        float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(slot) * 3 * a.C);
+        for (int64_t i = lo + lane; i < hi; i += 32) hdst[i] = __ldg(wsrc + i);
+    }
+    if (rbase >= D) return;  // d = 16: two warps hold no rows
+
+    const int kc = lane % DV4, ro = lane / DV4;
     float *sbase = a.ssm + (int64_t(slot) * a.Hv + h) * D * D;
-    float4 sv[RPT];
-    if (active) {
+    float4 sv[NF];
 #pragma unroll
-        for (int r = 0; r < RPT; ++r)
-            sv[r] = *reinterpret_cast<const float4 *>(sbase + (rg + GROUPS * r) * D + 4 * kc);
+    for (int f = 0; f < NF; ++f)
+        sv[f] = *reinterpret_cast<const float4 *>(sbase + (rbase + ro + RI * f) * D + 4 * kc);
+
+    // path, leaf first: lane i holds entry i (register lo) and i + 32 (hi)
+    const int p_lo = lane <= acc ? a.parents[n0 + lane] : -1;
+    const int p_hi = lane + 32 <= acc ? a.parents[n0 + lane + 32] : -1;
+    int node_lo = -1, node_hi = -1, m = 0;
+    for (int cur = acc; cur >= 0; ++m) {
+        if (lane == (m & 31)) {
+            if (m < 32) node_lo = cur; else node_hi = cur;
+        }
+        cur = __shfl_sync(full, cur < 32 ? p_lo : p_hi, cur & 31);
     }
-    __syncthreads();
-    const float gam = gam_s;
-    if (active) {
+    // coefficient of leaf-first entry i = product of the decays of entries 0..i-1
+    const float *dbase = a.replay + int64_t(h) * a.rstride + 2 * D;
+    const int64_t rnode = int64_t(a.Hv) * a.rstride;
+    const float d_lo = node_lo >= 0 ? __ldg(dbase + (int64_t(n0) + node_lo) * rnode) : 1.0f;
+    const float d_hi = node_hi >= 0 ? __ldg(dbase + (int64_t(n0) + node_hi) * rnode) : 1.0f;
+    float x_lo = d_lo, x_hi = d_hi;  // inclusive scans
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            sv[r].x *= gam; sv[r].y *= gam; sv[r].z *= gam; sv[r].w *= gam;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y_lo = __shfl_up_sync(full, x_lo, o), y_hi = __shfl_up_sync(full, x_hi, o);
+        if (lane >= o) {
+            x_lo *= y_lo;
+            x_hi *= y_hi;
         }
     }
-    for (int base = 0; base < m; base += kStage) {
-        const int cnt = min(kStage, m - base);
-        for (int idx = tid; idx < cnt * DV4; idx += kApplyThreads) {
-            const int j = idx / DV4, c4 = idx - j * DV4;
-            const float *row = a.replay + ((int64_t(n0) + path[base + j]) * a.Hv + h) * a.rstride;
-            const float cj = coef[base + j];
-            *reinterpret_cast<float4 *>(&kst[j][4 * c4]) = __ldg(reinterpret_cast<const float4 *>(row) + c4);
-            float4 uv = __ldg(reinterpret_cast<const float4 *>(row + D) + c4);
-            uv.x *= cj; uv.y *= cj; uv.z *= cj; uv.w *= cj;
-            *reinterpret_cast<float4 *>(&ust[j][4 * c4]) = uv;
-        }
-        __syncthreads();
-        if (active) {
-            for (int j = 0; j < cnt; ++j) {
-                const float4 kv = *reinterpret_cast<const float4 *>(&kst[j][4 * kc]);
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) {
-                    const float uj = ust[j][rg + GROUPS * r];
-                    sv[r].x = fmaf(uj, kv.x, sv[r].x);
-                    sv[r].y = fmaf(uj, kv.y, sv[r].y);
-                    sv[r].z = fmaf(uj, kv.z, sv[r].z);
-                    sv[r].w = fmaf(uj, kv.w, sv[r].w);
-                }
-            }
-        }
-        __syncthreads();
+    const float tot_lo = __shfl_sync(full, x_lo, 31);
+    float c_lo = __shfl_up_sync(full, x_lo, 1), c_hi = __shfl_up_sync(full, x_hi, 1);
+    if (lane == 0) {
+        c_lo = 1.0f;
+        c_hi = 1.0f;
     }
-    if (active) {
+    c_hi *= tot_lo;
+    const float gam = tot_lo * __shfl_sync(full, x_hi, 31);  // all m decays
+
 #pragma unroll
-        for (int r = 0; r < RPT; ++r)
-            *reinterpret_cast<float4 *>(sbase + (rg + GROUPS * r) * D + 4 * kc) = sv[r];
+    for (int f = 0; f < NF; ++f) {
+        sv[f].x *= gam; sv[f].y *= gam; sv[f].z *= gam; sv[f].w *= gam;
     }
-    // this head's share of the window copy: conv_hist[slot] <- win[accepted]
-    const int64_t total4 = int64_t(3) * a.C / 4;
-    const int64_t per = (total4 + a.Hv - 1) / a.Hv;
-    const int64_t lo = h * per, hi = min(total4, lo + per);
-    const float4 *wsrc = reinterpret_cast<const float4 *>(a.win + (int64_t(n0) + acc) * 3 * a.C);
-    float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(slot) * 3 * a.C);
-    for (int64_t i = lo + tid; i < hi; i += kApplyThreads) hdst[i] = __ldg(wsrc + i);
+    // one path step: k^_j (this lane's columns) and u_j (the warp's rows)
+    auto load_step = [&](int i, float4 &kv, float4 &ua, float4 &ub, float &cj) {
+        const int j = __shfl_sync(full, i < 32 ? node_lo : node_hi, i & 31);
+        cj = __shfl_sync(full, i < 32 ? c_lo : c_hi, i & 31);
+        const float *row = a.replay + ((int64_t(n0) + j) * a.Hv + h) * a.rstride;
+        kv = __ldg(reinterpret_cast<const float4 *>(row) + kc);
+        ua = __ldg(reinterpret_cast<const float4 *>(row + D + rbase));
+        ub = __ldg(reinterpret_cast<const float4 *>(row + D + rbase) + 1);
+    };
+    // root first: leaf-first entries m-1 .. 0, the next step's loads in flight
+    float4 kv, ua, ub, kn, un_a, un_b;
+    float cj, cn;
+    if (m > 0) load_step(m - 1, kv, ua, ub, cj);
+    for (int i = m - 1; i >= 0; --i) {
+        if (i > 0) load_step(i - 1, kn, un_a, un_b, cn);
+        const float uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+            // row rbase + ro + RI f
+            float uj = uw[RI * f];
+#pragma unroll
+            for (int qq = 1; qq < RI; ++qq)
+                if (ro == qq) uj = uw[RI * f + qq];
+            uj *= cj;
+            sv[f].x = fmaf(uj, kv.x, sv[f].x);
+            sv[f].y = fmaf(uj, kv.y, sv[f].y);
+            sv[f].z = fmaf(uj, kv.z, sv[f].z);
+            sv[f].w = fmaf(uj, kv.w, sv[f].w);
+        }
+        kv = kn; ua = un_a; ub = un_b; cj = cn;
+    }
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+        *reinterpret_cast<float4 *>(sbase + (rbase + ro + RI * f) * D + 4 * kc) = sv[f];
+
 }
 
 }  // namespace
@@ -220,12 +234,14 @@ extern "C" int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const i
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     commit_preflight_kernel<<<unsigned((S + 7) / 8), 256, 0, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_LAUNCH;
-    const dim3 grid{unsigned(Hv), unsigned(S)};
+    // CTAs of 32 state rows: d / 32 per head (one for d = 16)
+    const unsigned cph = unsigned((D + kCtaRows - 1) / kCtaRows);
+    const dim3 grid{unsigned(Hv) * cph, unsigned(S)};
     switch (D) {
-        case 16: commit_apply_kernel<16><<<grid, kApplyThreads, 0, st>>>(a); break;
-        case 32: commit_apply_kernel<32><<<grid, kApplyThreads, 0, st>>>(a); break;
-        case 64: commit_apply_kernel<64><<<grid, kApplyThreads, 0, st>>>(a); break;
-        default: commit_apply_kernel<128><<<grid, kApplyThreads, 0, st>>>(a); break;
+        case 16: commit_apply_warp_kernel<16><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
+        case 32: commit_apply_warp_kernel<32><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
+        case 64: commit_apply_warp_kernel<64><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
+        default: commit_apply_warp_kernel<128><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }

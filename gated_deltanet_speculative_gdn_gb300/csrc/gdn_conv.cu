@@ -8,19 +8,21 @@
 // in llama-cpp-bonsai "llama-cpp-bonsai-gdn-conv.patch" (ssm_conv_concat
 // kernel): history columns first, taps summed j = 0..3 from the oldest.
 //
-// Layout: one CTA per (sequence, block of 512 channels); each thread owns four
-// adjacent channels and walks the sequence's nodes in order.  The parent walk
-// of every node (three columns back, into the history above the root) is
-// resolved once per CTA in shared memory.  Loads and stores are 128-bit and
-// coalesced; an ancestor's token row was loaded by this CTA moments earlier
-// and is served from L1.  HBM-bound: per node it reads one token row and
-// writes xc (one row) and the window (three rows).
+// Layout: one CTA of four warps per (sequence, block of 128 channels); lane l
+// owns channels 4l..4l+3 of the block and warp w takes nodes w, w+4, w+8, ...
+// The parent walk of every node (three columns back, into the history above
+// the root) is resolved once per CTA in shared memory.  Loads and stores are
+// 128-bit and coalesced (512 contiguous bytes per warp); an ancestor's token
+// row is read by several warps of the CTA and served from L1/L2.  HBM-bound:
+// per node it reads one token row and writes xc (one row) and the window
+// (three rows).
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
 namespace {
 
-constexpr int kConvThreads = 128;  // x 4 channels = 512 channels per CTA
+constexpr int kConvThreads = 128;  // 4 warps; 32 lanes x 4 channels = 128 channels per CTA
+constexpr int kConvChannels = 128;
 
 struct ConvArgs {
     const float *__restrict__ x;
@@ -93,7 +95,8 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
     }
     __syncthreads();
 
-    const int c4 = blockIdx.x * kConvThreads + tid;  // float4 channel group
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c4 = blockIdx.x * (kConvChannels / 4) + lane;  // float4 channel group
     if (4 * c4 >= a.C) return;
     const int64_t C = a.C;
     const float4 *w4 = reinterpret_cast<const float4 *>(a.w) + 4 * static_cast<int64_t>(c4);
@@ -110,10 +113,9 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
         return tap == 2 ? h2 : (tap == 1 ? h1 : h0);
     };
 
-#pragma unroll 2
-    for (int i = 0; i < ns; ++i) {
-        const int n = n0 + i;
-        const float4 c0 = column(n);         // x(t), newest
+    for (int i = warp; i < ns; i += kConvThreads / 32) {
+        const int64_t n = n0 + i;
+        const float4 c0 = column(n0 + i);     // x(t), newest
         const float4 c1 = column(src[i][0]);
         const float4 c2 = column(src[i][1]);
         const float4 c3 = column(src[i][2]);  // oldest of the window
@@ -123,8 +125,8 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
         acc.y = fmaf(c0.y, wc1.w, fmaf(c1.y, wc1.z, fmaf(c2.y, wc1.y, fmaf(c3.y, wc1.x, 0.0f))));
         acc.z = fmaf(c0.z, wc2.w, fmaf(c1.z, wc2.z, fmaf(c2.z, wc2.y, fmaf(c3.z, wc2.x, 0.0f))));
         acc.w = fmaf(c0.w, wc3.w, fmaf(c1.w, wc3.z, fmaf(c2.w, wc3.y, fmaf(c3.w, wc3.x, 0.0f))));
-        *reinterpret_cast<float4 *>(a.xc + static_cast<int64_t>(n) * C + 4 * c4) = silu4(acc);
-        float *wrow = a.win + static_cast<int64_t>(n) * 3 * C + 4 * c4;
+        *reinterpret_cast<float4 *>(a.xc + n * C + 4 * c4) = silu4(acc);
+        float *wrow = a.win + n * 3 * C + 4 * c4;
         // the windows are read back only for the accepted node: stream them past L2
         __stcs(reinterpret_cast<float4 *>(wrow), c2);
         __stcs(reinterpret_cast<float4 *>(wrow + C), c1);
@@ -164,7 +166,7 @@ extern "C" int gdn_conv_tree_step(const gdn_dims *dims, const float *x, int64_t 
     ConvArgs a{x, x_stride, conv_w, conv_hist, parents, node_off, slot_map, xc, win, status,
                int(S), int(N), int(P), int(C), dims->max_seq_nodes};
     const int c4 = int(C / 4);
-    const dim3 grid{unsigned((c4 + kConvThreads - 1) / kConvThreads), unsigned(S)};
+    const dim3 grid{unsigned((c4 + kConvChannels / 4 - 1) / (kConvChannels / 4)), unsigned(S)};
     conv_tree_step_kernel<<<grid, kConvThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }

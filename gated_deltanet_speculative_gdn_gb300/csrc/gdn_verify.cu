@@ -36,6 +36,8 @@
 // the same dense form.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
@@ -393,112 +395,141 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
 }
 
 // ============================================================================
-// Tensor-core variant for d = 128 and trees of at most 16 nodes.
+// Tensor-core variant for d = 128 and trees of at most 16 nodes: a persistent,
+// warp-specialised pipeline.
 //
-// The contraction D[i][c] = sum_k S0[i][k] B[c][k], with B = [k^_0..k^_15 |
-// q^_0..q^_15] (unscaled), is a 128 x 32 x 128 matrix product per (sequence,
-// head).  It runs on tcgen05 with the accumulators in tensor memory, in three
-// tf32 products that recover fp32 accuracy (x = hi + lo, hi = x with the low
-// 13 mantissa bits cleared, lo exact):
+// Per (sequence, value head) "item" the contraction
+//     D[i][c] = sum_k S0[i][k] B[c][k],   B = [k^_0..k^_15 | q^_0..q^_15] (unscaled)
+// is a 128 x 32 x 128 matrix product.  It runs on tcgen05 with accumulators in
+// tensor memory, as three tf32 products that recover fp32 accuracy (x = hi +
+// lo, hi = x with the low 13 mantissa bits cleared, lo exact):
 //     D = A_hi B_hi + A_hi B_lo + A_lo B_hi      (the dropped A_lo B_lo ~ 2^-22)
-// The tensor cores align and truncate when they accumulate, so the large
-// A_hi B_hi term of each K-chunk gets an accumulator of its own and the two
-// small terms share one more; the epilogue adds them in fp32.
-// S0 streams through a two-slot ring of 16 KB K-chunks ([128 rows][32 floats],
-// TMA, 128-byte swizzle, which is also the tensor cores' K-major operand
-// layout); the CTA splits each chunk into hi (in place) and lo, one thread
-// issues the chunk's 12 MMAs, and the chunk after next is loaded into the slot
-// once the MMAs that read it have completed.  The path coefficients need only
-// the dot products along each node's ancestor path: each warp holds the k^ and
-// q^ of its four nodes in registers and forms them with shuffle reductions.
-// Gamma_t scales column t in the epilogue, where thread i reads row i of the
-// accumulators straight from tensor memory.  ~100 KB of shared memory: two
-// CTAs per SM.
-namespace tcv {
+// The tensor cores align and truncate when they accumulate, so the A_hi B_hi
+// term of each K-chunk gets an accumulator of its own and the two small terms
+// share one; the epilogue adds them in fp32.
+//
+// One CTA per SM walks a list of items.  Warp roles:
+//   warp 0       TMA producer: streams each item's S0 as four 16 KB K-chunks
+//                ([128 rows][32 floats], 128-byte swizzle = the tensor cores'
+//                K-major operand layout) into a four-slot ring;
+//   warp 1       MMA issuer: once a chunk is split and the item's B is ready,
+//                issues the chunk's 12 MMAs into the item's team accumulators;
+//   warps 2-5    team 0 and warps 6-9 team 1, on alternate items: q/k/v and
+//                gates, B = normalised q/k split into hi/lo, the split of each
+//                S0 chunk (hi in place, lo beside it), the path coefficients
+//                (dot products along each node's ancestors, shuffle-reduced),
+//                and the per-row epilogue reading the accumulators from tensor
+//                memory (thread i owns state row i).
+// While one team runs an item's epilogue the other prepares the next item and
+// the producer keeps the ring full, so loads, tensor-core work and CUDA-core
+// work of different items overlap.
+namespace wsv {
 constexpr int D = 128;
-constexpr uint32_t kChunk = 128 * 128;        // bytes of one S0 K-chunk
-constexpr uint32_t kBChunk = 32 * 128;        // bytes of one B K-chunk
-constexpr uint32_t RAW = 0;                   // 2 slots: S0 chunk, hi in place
-constexpr uint32_t LO = RAW + 2 * kChunk;     // 2 slots: lo of the chunk
-constexpr uint32_t BHI = LO + 2 * kChunk;     // B hi, 4 K-chunks
-constexpr uint32_t BLO = BHI + 4 * kBChunk;   // B lo
-constexpr uint32_t SMALL = BLO + 4 * kBChunk;
-// float offsets inside the small area
-constexpr int CK = 0, CQ = CK + 256, BETA = CQ + 256, DEC = BETA + 16, GAM = DEC + 16, PAR = GAM + 16,
-              BARS = PAR + 16, TMEMA = BARS + 8, SMALL_FLOATS = TMEMA + 4;
-constexpr size_t BYTES = SMALL + SMALL_FLOATS * 4 + 1024;
-// instruction descriptor: D fp32, A and B tf32, both K-major, M = 128, N = 32
+constexpr int kWarps = 10;
+constexpr int kThreadsWS = kWarps * 32;
+constexpr int kMaxItems = 64;                    // items per CTA
+constexpr uint32_t kChunk = 128 * 128;           // bytes of one S0 K-chunk
+constexpr uint32_t kBChunk = 32 * 128;           // bytes of one B K-chunk
+constexpr uint32_t kBTeam = 4 * kBChunk;         // one team's B (hi or lo)
+constexpr uint32_t RAW = 0;                      // 4 ring slots: S0 chunk, hi in place
+constexpr uint32_t LO = RAW + 4 * kChunk;        // 4 ring slots: lo of the chunk
+constexpr uint32_t BHI = LO + 4 * kChunk;        // per team
+constexpr uint32_t BLO = BHI + 2 * kBTeam;       // per team
+constexpr uint32_t SMALL = BLO + 2 * kBTeam;
+// per-team small area (4-byte words)
+constexpr int T_CK = 0, T_CQ = 256, T_BETA = 512, T_DEC = 528, T_GAM = 544, T_PAR = 560, T_WORDS = 576;
+// CTA-wide words after the two team areas
+constexpr int W_BARS = 2 * T_WORDS;              // 22 mbarriers (8 B each)
+constexpr int W_TMEM = W_BARS + 44;
+constexpr int W_ABORT = W_TMEM + 1;
+constexpr int W_NV = W_ABORT + 1;
+constexpr int W_LIST = W_NV + 2;                 // kMaxItems x int4 (item, n0, ns, slot), 16-B aligned
+constexpr int SMALL_WORDS = W_LIST + 4 * kMaxItems;
+constexpr size_t BYTES = SMALL + SMALL_WORDS * 4 + 1024;
+// barrier indices
+// B_FULL + 4 t + kb: chunk kb of team t's current item landed (a team sees
+// every phase of its own barriers, never the other team's)
+constexpr int B_FULL = 0, B_SPLIT = 8, B_EMPTY = 12, B_BREADY = 16, B_ACCFULL = 18, B_ACCEMPTY = 20, N_BARS = 22;
 constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-// columns 32 kb: A_hi B_hi of K-chunk kb; columns 128..159: the two small terms
-constexpr uint32_t TMEM_COLS = 256, SMALL_COL = 128;
+// team t: columns 256 t + 32 kb (A_hi B_hi of chunk kb) and 256 t + 128 (small terms)
+constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256, SMALL_COL = 128;
 
-// byte offset of element k of row `row` in a [rows][32 floats]-per-chunk,
-// 128-byte-swizzled, K-major buffer (chunk size `chunk` bytes)
 __device__ __forceinline__ uint32_t sw_off(int row, int k, uint32_t chunk) {
     return uint32_t(k >> 5) * chunk + uint32_t(row) * 128u + ((uint32_t(((k & 31) >> 2) ^ (row & 7))) << 4) +
            uint32_t(k & 3) * 4u;
 }
-
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
     return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
-}  // namespace tcv
+__device__ __forceinline__ void team_sync(int team) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(128) : "memory");
+}
+// A wait that gives up at once after any role has timed out (the CTA then
+// drains and exits), and otherwise waits at most the library's wait limit.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (*abort_flag) return false;
+    if (gdn::mbar_wait_bounded(bar, parity)) return true;
+    *abort_flag = 1;
+    return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gdn::smem_addr(bar)) : "memory");
+}
+}  // namespace wsv
 
-__global__ void __launch_bounds__(kThreads, 2)
-    tree_verify_tc_kernel(const __grid_constant__ CUtensorMap tmap, const VerifyArgs a) {
-    using namespace tcv;
+__global__ void __launch_bounds__(wsv::kThreadsWS, 1)
+    tree_verify_ws_kernel(const __grid_constant__ CUtensorMap tmap, const VerifyArgs a) {
+    using namespace wsv;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sb =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = gdn::smem_addr(sb);
-    float *small = reinterpret_cast<float *>(sb + SMALL);
-    float *cks = small + CK, *cqs = small + CQ;
-    float *beta_s = small + BETA, *dec_s = small + DEC, *gam_s = small + GAM;
-    int *par = reinterpret_cast<int *>(small + PAR);
-    uint64_t *full = reinterpret_cast<uint64_t *>(small + BARS);  // [2] chunk landed
-    uint64_t *mmab = full + 2;                                     // [2] chunk's MMAs done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + TMEMA);
-    __shared__ int hdr[4];  // error, first node, node count, slot
+    int *words = reinterpret_cast<int *>(sb + SMALL);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(words + W_BARS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(words + W_TMEM);
+    volatile int *abort_flag = words + W_ABORT;
+    int4 *list = reinterpret_cast<int4 *>(words + W_LIST);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.x, s = blockIdx.y;
-    const int kh = h / (a.Hv / a.Hk);
+    const int total = a.S * a.Hv;
 
-    if (tid == 0) {
-        const int n0 = a.node_off[s], n1 = a.node_off[s + 1];
-        int err = 0;
-        if (n0 < 0 || n1 < n0 || n1 > a.N || (s == 0 && n0 != 0) || (s == a.S - 1 && n1 != a.N) ||
-            n1 - n0 > a.max_nodes || n1 - n0 > kSeg)
-            err = GDN_DEV_BAD_NODE_OFF;
-        const int slot = a.slot_map[s];
-        if (!err && (slot < 0 || slot >= a.P)) err = GDN_DEV_BAD_SLOT;
-        hdr[0] = err;
-        hdr[1] = n0;
-        hdr[2] = n1 - n0;
-        hdr[3] = slot;
-    }
-    __syncthreads();
-    if (hdr[0] || hdr[2] == 0) {
-        if (tid == 0 && hdr[0]) gdn::record_status(a.status, hdr[0]);
-        return;
-    }
-    const int n0 = hdr[1], lc = hdr[2], slot = hdr[3];
-    if (tid < lc) {
-        const int p = a.parents[n0 + tid];
-        par[tid] = p;
-        if (p < -1 || p >= tid) hdr[0] = GDN_DEV_BAD_PARENT;
-    }
-    __syncthreads();
-    if (hdr[0]) {
-        if (tid == 0) gdn::record_status(a.status, hdr[0]);
-        return;
-    }
-    // ---- set-up: barriers, tensor memory, first two S0 chunks ---------------
-    if (tid == 0) {
-        for (int i = 0; i < 4; ++i) gdn::mbar_init(full + i, 1);
-        gdn::fence_mbar_init();
-    }
+    // ---- set-up: this CTA's valid items, barriers, tensor memory -------------
     if (warp == 0) {
+        int nv = 0;
+        for (int k0 = 0; k0 < kMaxItems; k0 += 32) {
+            const int it = blockIdx.x + (k0 + lane) * gridDim.x;
+            int n0 = 0, ns = 0, slot = 0, err = 0;
+            if (k0 + lane < kMaxItems && it < total) {
+                const int s = it / a.Hv;
+                n0 = a.node_off[s];
+                const int n1 = a.node_off[s + 1];
+                slot = a.slot_map[s];
+                ns = n1 - n0;
+                if (n0 < 0 || n1 < n0 || n1 > a.N || (s == 0 && n0 != 0) || (s == a.S - 1 && n1 != a.N) ||
+                    ns > a.max_nodes || ns > kSeg)
+                    err = GDN_DEV_BAD_NODE_OFF;
+                else if (ns > 0 && (slot < 0 || slot >= a.P))
+                    err = GDN_DEV_BAD_SLOT;
+                if (err) gdn::record_status(a.status, err);
+            }
+            const bool valid = k0 + lane < kMaxItems && it < total && !err && ns > 0;
+            const unsigned m = __ballot_sync(0xffffffffu, valid);
+            if (valid) list[nv + __popc(m & ((1u << lane) - 1u))] = make_int4(it, n0, ns, slot);
+            nv += __popc(m);
+        }
+        if (lane == 0) words[W_NV] = nv;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < N_BARS; ++i) {
+            const bool by_team = (i >= B_SPLIT && i < B_EMPTY) || (i >= B_BREADY && i < B_ACCFULL) ||
+                                 i >= B_ACCEMPTY;
+            const uint32_t cnt = by_team ? 128u : 1u;
+            gdn::mbar_init(bars + i, cnt);
+        }
+        gdn::fence_mbar_init();
+        *abort_flag = 0;
+    }
+    if (warp == 1) {
         gdn::tmem_alloc(tmem_slot, TMEM_COLS);
         gdn::tmem_relinquish();
     }
@@ -506,213 +537,286 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     gdn::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int ybox = (slot * a.Hv + h) * D;
-    if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            gdn::mbar_arrive_expect_tx(full + b, kChunk);
-            gdn::tma_load_2d(sb + RAW + b * kChunk, &tmap, 32 * b, ybox, full + b);
-        }
-    }
+    const int nv = words[W_NV];
 
-    // ---- A: v of this row, gates, normalised q and k into B (hi / lo) --------
-    const int64_t C = a.C;
-    const int qoff = kh * D, koff = a.Hk * D + kh * D, voff = 2 * a.Hk * D + h * D;
-    float vreg[kSeg];
-#pragma unroll
-    for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? __ldg(a.xc + (n0 + t) * C + voff + tid) : 0.0f;
-    if (warp == 0 && lane < lc) {
-        const int64_t n = n0 + lane;
-        const float bv = __ldg(a.ba + n * a.ba_stride + h);
-        const float av = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
-        const float dec = expf(gdn::softplus_f(av + a.dt_bias[h]) * a.A[h]);
-        beta_s[lane] = gdn::sigmoid_f(bv);
-        dec_s[lane] = dec;
-        a.replay[(n * a.Hv + h) * a.rstride + 2 * D] = dec;
-    }
-    // warp w normalises B rows c = w + 4 j: k^ of nodes w, w+4, w+8, w+12
-    // (j < 4) and q^ of the same nodes (j >= 4); lane l holds elements 4l..4l+3
-    float4 nv[8];
-    {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int c = warp + 4 * j, t = c & 15;
-            nv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < lc)
-                nv[j] = __ldg(reinterpret_cast<const float4 *>(a.xc + (n0 + t) * C + (c < kSeg ? koff : qoff) +
-                                                               4 * lane));
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int c = warp + 4 * j, t = c & 15;
-            float ss = nv[j].x * nv[j].x;
-            ss = fmaf(nv[j].y, nv[j].y, ss);
-            ss = fmaf(nv[j].z, nv[j].z, ss);
-            ss = fmaf(nv[j].w, nv[j].w, ss);
-            ss = gdn::warp_sum(ss);
-            nv[j] = scale4(nv[j], rsqrtf(ss + 1e-6f));
-            const float4 hi = make_float4(gdn::tf32_hi(nv[j].x), gdn::tf32_hi(nv[j].y), gdn::tf32_hi(nv[j].z),
-                                          gdn::tf32_hi(nv[j].w));
-            const float4 lo = make_float4(nv[j].x - hi.x, nv[j].y - hi.y, nv[j].z - hi.z, nv[j].w - hi.w);
-            const uint32_t off = sw_off(c, 4 * lane, kBChunk);
-            *reinterpret_cast<float4 *>(sb + BHI + off) = hi;
-            *reinterpret_cast<float4 *>(sb + BLO + off) = lo;
-            if (c < kSeg && t < lc)
-                *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride + 4 * lane) =
-                    nv[j];
-        }
-    }
-    gdn::fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- C: path coefficients and Gamma; warp w handles its own four nodes ---
-    // For node t and each ancestor j (walking up), with gamma = the decays
-    // strictly after j up to t:  cks[t][j] = gamma k^_j . k^_t,
-    // cqs[t][j] = gamma k^_j . q^_t;  cqs[t][t] = k^_t . q^_t;  Gamma_t = all decays.
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const int t = warp + 4 * jj;
-        if (t < lc) {
-            const float4 kt = nv[jj], qt = nv[4 + jj];
-            float ck = 0.f, cq = 0.f;  // lane j < 16 owns entry j of row t
-            const float self = gdn::warp_sum(gdn::fma4(kt, qt, 0.f));
-            if (lane == t) cq = self;
-            float gam = dec_s[t];
-            for (int j = par[t]; j >= 0; j = par[j]) {
-                const uint32_t oj = sw_off(j, 4 * lane, kBChunk);
-                const float4 kj = add4(*reinterpret_cast<const float4 *>(sb + BHI + oj),
-                                       *reinterpret_cast<const float4 *>(sb + BLO + oj));
-                const float kk = gdn::warp_sum(gdn::fma4(kj, kt, 0.f));
-                const float kq = gdn::warp_sum(gdn::fma4(kj, qt, 0.f));
-                if (lane == j) {
-                    ck = gam * kk;
-                    cq = gam * kq;
+    if (warp == 0) {
+        // ---- producer: four S0 chunks per item into ring slots 0..3 -----------
+        if (lane == 0) {
+            for (int v = 0; v < nv; ++v) {
+                const int4 e = list[v];
+                const int y = (e.w * a.Hv + e.x % a.Hv) * D;
+                for (int kb = 0; kb < 4; ++kb) {
+                    if (v > 0 && !wait_or_abort(bars + B_EMPTY + kb, uint32_t((v - 1) & 1), abort_flag)) break;
+                    uint64_t *fb = bars + B_FULL + 4 * (v & 1) + kb;
+                    gdn::mbar_arrive_expect_tx(fb, kChunk);
+                    gdn::tma_load_2d(sb + RAW + kb * kChunk, &tmap, 32 * kb, y, fb);
                 }
-                gam *= dec_s[j];
+                if (*abort_flag) break;
             }
-            if (lane < kSeg) {
-                cks[t * kSeg + lane] = ck;
-                cqs[t * kSeg + lane] = cq;
-            }
-            if (lane == 0) gam_s[t] = gam;
         }
-    }
-
-    // ---- D: S0 chunks through the ring, 3 x tf32 MMAs per K-step -------------
-    bool ok = true;
-    for (int kb = 0; kb < 4; ++kb) {
-        const int sl = kb & 1;
-        if (!gdn::mbar_wait_bounded(full + sl, uint32_t(kb >> 1))) hdr[0] = GDN_DEV_TIMEOUT;
-        float4 *raw = reinterpret_cast<float4 *>(sb + RAW + sl * kChunk);
-        float4 *lo = reinterpret_cast<float4 *>(sb + LO + sl * kChunk);
-#pragma unroll
-        for (int j = 0; j < int(kChunk / 16 / kThreads); ++j) {
-            const int f = tid + kThreads * j;
-            const float4 x = raw[f];
-            const float4 hi = make_float4(gdn::tf32_hi(x.x), gdn::tf32_hi(x.y), gdn::tf32_hi(x.z),
-                                          gdn::tf32_hi(x.w));
-            raw[f] = hi;
-            lo[f] = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
-        }
-        gdn::fence_proxy_async_smem();
-        __syncthreads();
-        if (hdr[0]) {
-            ok = false;
-            break;
-        }
-        if (tid == 0) {
-            gdn::tc_fence_after_sync();
-            const uint32_t dbig = tmem + 32u * kb;
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ahi = gdn::desc_sw128(sbase + RAW + sl * kChunk + ks * 32);
-                const uint64_t alo = gdn::desc_sw128(sbase + LO + sl * kChunk + ks * 32);
-                const uint64_t bhi = gdn::desc_sw128(sbase + BHI + kb * kBChunk + ks * 32);
-                const uint64_t blo = gdn::desc_sw128(sbase + BLO + kb * kBChunk + ks * 32);
-                gdn::mma_tf32(dbig, ahi, bhi, IDESC, ks != 0);
-                gdn::mma_tf32(tmem + SMALL_COL, ahi, blo, IDESC, (kb | ks) != 0);
-                gdn::mma_tf32(tmem + SMALL_COL, alo, bhi, IDESC, 1);
-            }
-            gdn::mma_commit(mmab + sl);
-            if (kb < 2) {
-                // the slot is free once the MMAs reading it have completed
-                if (gdn::mbar_wait_bounded(mmab + sl, 0)) {
-                    gdn::mbar_arrive_expect_tx(full + sl, kChunk);
-                    gdn::tma_load_2d(sb + RAW + sl * kChunk, &tmap, 32 * (kb + 2), ybox, full + sl);
-                } else {
-                    hdr[0] = GDN_DEV_TIMEOUT;
+    } else if (warp == 1) {
+        // ---- MMA issuer --------------------------------------------------------
+        if (lane == 0) {
+            for (int v = 0; v < nv; ++v) {
+                const int t = v & 1, ut = v >> 1;
+                if (!wait_or_abort(bars + B_BREADY + t, uint32_t(ut & 1), abort_flag)) break;
+                if (ut > 0 && !wait_or_abort(bars + B_ACCEMPTY + t, uint32_t((ut - 1) & 1), abort_flag)) break;
+                const uint32_t dacc = tmem + TEAM_COLS * t;
+                bool ok = true;
+                for (int kb = 0; kb < 4 && ok; ++kb) {
+                    if (!wait_or_abort(bars + B_SPLIT + kb, uint32_t(v & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    gdn::tc_fence_after_sync();
+                    uint64_t ahi = gdn::desc_sw128(sbase + RAW + kb * kChunk);
+                    uint64_t alo = gdn::desc_sw128(sbase + LO + kb * kChunk);
+                    uint64_t bhi = gdn::desc_sw128(sbase + BHI + t * kBTeam + kb * kBChunk);
+                    uint64_t blo = gdn::desc_sw128(sbase + BLO + t * kBTeam + kb * kBChunk);
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks, ahi += 2, alo += 2, bhi += 2, blo += 2) {
+                        gdn::mma_tf32(dacc + 32u * kb, ahi, bhi, IDESC, ks != 0);
+                        gdn::mma_tf32(dacc + SMALL_COL, ahi, blo, IDESC, (kb | ks) != 0);
+                        gdn::mma_tf32(dacc + SMALL_COL, alo, bhi, IDESC, 1);
+                    }
+                    gdn::mma_commit(bars + B_EMPTY + kb);
                 }
-            }
-        }
-    }
-
-    if (ok) {
-        // the last commit covers every MMA of the CTA
-        if (!gdn::mbar_wait_bounded(mmab + 1, 1)) hdr[0] = GDN_DEV_TIMEOUT;
-        __syncthreads();
-        ok = hdr[0] == 0;
-    }
-    if (ok) {
-        gdn::tc_fence_after_sync();
-        const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-        float dv[32];
-        {
-            float p1[32];
-            gdn::tmem_ld32(trow + 0, dv);
-            gdn::tmem_ld32(trow + 32, p1);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dv[i] += p1[i];
-            float p2[32];
-            gdn::tmem_ld32(trow + 64, p1);
-            gdn::tmem_ld32(trow + 96, p2);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dv[i] += p1[i] + p2[i];
-            gdn::tmem_ld32(trow + SMALL_COL, p1);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dv[i] += p1[i];
-        }
-
-        // ---- E: per row, the nodes in order ----------------------------------
-        float u[kSeg];
-#pragma unroll
-        for (int t = 0; t < kSeg; ++t) {
-            u[t] = 0.f;
-            if (t < lc) {
-                const int64_t n = n0 + t;
-                float sk = gam_s[t] * dv[t];
-                float oq = gam_s[t] * dv[kSeg + t];
-#pragma unroll
-                for (int j4 = 0; j4 < (t + 4) / 4; ++j4) {
-                    const float4 ckv = *reinterpret_cast<const float4 *>(cks + t * kSeg + 4 * j4);
-                    const float4 cqv = *reinterpret_cast<const float4 *>(cqs + t * kSeg + 4 * j4);
-                    if (4 * j4 + 0 < t) sk = fmaf(ckv.x, u[4 * j4 + 0], sk);
-                    if (4 * j4 + 1 < t) sk = fmaf(ckv.y, u[4 * j4 + 1], sk);
-                    if (4 * j4 + 2 < t) sk = fmaf(ckv.z, u[4 * j4 + 2], sk);
-                    if (4 * j4 + 3 < t) sk = fmaf(ckv.w, u[4 * j4 + 3], sk);
-                    if (4 * j4 + 0 < t) oq = fmaf(cqv.x, u[4 * j4 + 0], oq);
-                    if (4 * j4 + 1 < t) oq = fmaf(cqv.y, u[4 * j4 + 1], oq);
-                    if (4 * j4 + 2 < t) oq = fmaf(cqv.z, u[4 * j4 + 2], oq);
-                    if (4 * j4 + 3 < t) oq = fmaf(cqv.w, u[4 * j4 + 3], oq);
-                }
-                u[t] = beta_s[t] * (vreg[t] - sk);
-                oq = fmaf(cqs[t * kSeg + t], u[t], oq);
-                a.o[(n * a.Hv + h) * D + tid] = a.q_scale * oq;
-                a.replay[(n * a.Hv + h) * a.rstride + D + tid] = u[t];
+                if (!ok) break;
+                gdn::mma_commit(bars + B_ACCFULL + t);
             }
         }
     } else {
-        // a wait ran out: drain what may still be in flight (bounded) before
-        // the shared and tensor memory are released
+        // ---- math teams ----------------------------------------------------------
+        const int team = (warp - 2) >> 2, tw = (warp - 2) & 3;   // warp within the team
+        const int ttid = tw * 32 + lane;                          // 0..127
+        const int row = (warp & 3) * 32 + lane;                   // tensor-memory lane = state row
+        int *tws = words + team * T_WORDS;
+        float *cks = reinterpret_cast<float *>(tws + T_CK), *cqs = reinterpret_cast<float *>(tws + T_CQ);
+        float *beta_s = reinterpret_cast<float *>(tws + T_BETA), *dec_s = reinterpret_cast<float *>(tws + T_DEC);
+        float *gam_s = reinterpret_cast<float *>(tws + T_GAM);
+        int *par = tws + T_PAR;
+        unsigned char *bhi_t = sb + BHI + team * kBTeam, *blo_t = sb + BLO + team * kBTeam;
+        const int64_t C = a.C;
+
+        for (int v = team; v < nv; v += 2) {
+            const int ut = v >> 1;
+            const int4 e = list[v];
+            const int s = e.x / a.Hv, h = e.x % a.Hv, n0 = e.y, lc = e.z;
+            const int kh = h / (a.Hv / a.Hk);
+            const int qoff = kh * D, koff = a.Hk * D + kh * D, voff = 2 * a.Hk * D + h * D;
+            (void)s;
+            // the team's previous epilogue has finished reading the small area
+            team_sync(team);
+            // ---- A: parents, gates, normalised q and k into B (hi / lo) ----------
+            if (ttid < lc) {
+                int p = a.parents[n0 + ttid];
+                if (p < -1 || p >= ttid) {
+                    gdn::record_status(a.status, GDN_DEV_BAD_PARENT);
+                    p = -1;  // outputs of a failed call are unspecified; keep the walk in bounds
+                }
+                par[ttid] = p;
+            }
+            if (tw == 0 && lane < lc) {
+                const int64_t n = n0 + lane;
+                const float bv = __ldg(a.ba + n * a.ba_stride + h);
+                const float av = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
+                const float dec = expf(gdn::softplus_f(av + a.dt_bias[h]) * a.A[h]);
+                beta_s[lane] = gdn::sigmoid_f(bv);
+                dec_s[lane] = dec;
+                a.replay[(n * a.Hv + h) * a.rstride + 2 * D] = dec;
+            }
+            // warp tw normalises B rows c = tw + 4 j: k^ of nodes tw + 4 j (j < 4)
+            // and q^ of the same nodes (j >= 4); lane l holds elements 4l..4l+3
+            float4 nvv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = tw + 4 * j, t = c & 15;
+                nvv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < lc)
+                    nvv[j] = __ldg(reinterpret_cast<const float4 *>(a.xc + (n0 + t) * C + (c < kSeg ? koff : qoff) +
+                                                                    4 * lane));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = tw + 4 * j, t = c & 15;
+                float ss = nvv[j].x * nvv[j].x;
+                ss = fmaf(nvv[j].y, nvv[j].y, ss);
+                ss = fmaf(nvv[j].z, nvv[j].z, ss);
+                ss = fmaf(nvv[j].w, nvv[j].w, ss);
+                ss = gdn::warp_sum(ss);
+                nvv[j] = scale4(nvv[j], rsqrtf(ss + 1e-6f));
+                const float4 hi = make_float4(gdn::tf32_hi(nvv[j].x), gdn::tf32_hi(nvv[j].y),
+                                              gdn::tf32_hi(nvv[j].z), gdn::tf32_hi(nvv[j].w));
+                const float4 lo =
+                    make_float4(nvv[j].x - hi.x, nvv[j].y - hi.y, nvv[j].z - hi.z, nvv[j].w - hi.w);
+                const uint32_t off = sw_off(c, 4 * lane, kBChunk);
+                *reinterpret_cast<float4 *>(bhi_t + off) = hi;
+                *reinterpret_cast<float4 *>(blo_t + off) = lo;
+                if (c < kSeg && t < lc)
+                    *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride +
+                                                4 * lane) = nvv[j];
+            }
+            gdn::fence_proxy_async_smem();
+            mbar_arrive(bars + B_BREADY + team);
+
+            // ---- split the item's four S0 chunks as they land --------------------
+            for (int kb = 0; kb < 4; ++kb) {
+                if (!wait_or_abort(bars + B_FULL + 4 * team + kb, uint32_t(ut & 1), abort_flag)) continue;
+                float4 *raw = reinterpret_cast<float4 *>(sb + RAW + kb * kChunk);
+                float4 *lo = reinterpret_cast<float4 *>(sb + LO + kb * kChunk);
+#pragma unroll
+                for (int j = 0; j < int(kChunk / 16 / 128); ++j) {
+                    const int f = ttid + 128 * j;
+                    const float4 x = raw[f];
+                    const float4 hi = make_float4(gdn::tf32_hi(x.x), gdn::tf32_hi(x.y), gdn::tf32_hi(x.z),
+                                                  gdn::tf32_hi(x.w));
+                    raw[f] = hi;
+                    lo[f] = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+                }
+                gdn::fence_proxy_async_smem();
+                mbar_arrive(bars + B_SPLIT + kb);
+            }
+            team_sync(team);  // parents and decays written by other warps of the team
+
+            // ---- C: path coefficients and Gamma; warp tw handles nodes tw + 4 m ---
+            // For node t and each ancestor j (walking up), with gamma = the decays
+            // strictly after j up to t:  cks[t][j] = gamma k^_j . k^_t,
+            // cqs[t][j] = gamma k^_j . q^_t;  cqs[t][t] = k^_t . q^_t;  Gamma_t = the
+            // product of all its decays.  Lane j < 16 owns entry j of each row.
+            {
+                int cur[4];
+                float gam[4], ck[4], cq[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int t = tw + 4 * m;
+                    const bool valid = t < lc;
+                    const float self = gdn::warp_sum(gdn::fma4(nvv[m], nvv[4 + m], 0.f));
+                    cur[m] = valid ? par[t] : -1;
+                    gam[m] = valid ? dec_s[t] : 0.f;
+                    ck[m] = 0.f;
+                    cq[m] = (valid && lane == t) ? self : 0.f;
+                }
+                // the AND of the cursors is negative only once every one of them is -1
+                while ((cur[0] & cur[1] & cur[2] & cur[3]) >= 0) {
+                    float kk[4], kq[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        kk[m] = 0.f;
+                        kq[m] = 0.f;
+                        if (cur[m] >= 0) {
+                            const uint32_t oj = sw_off(cur[m], 4 * lane, kBChunk);
+                            const float4 kj = add4(*reinterpret_cast<const float4 *>(bhi_t + oj),
+                                                   *reinterpret_cast<const float4 *>(blo_t + oj));
+                            kk[m] = gdn::fma4(kj, nvv[m], 0.f);
+                            kq[m] = gdn::fma4(kj, nvv[4 + m], 0.f);
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            kk[m] += __shfl_xor_sync(0xffffffffu, kk[m], o);
+                            kq[m] += __shfl_xor_sync(0xffffffffu, kq[m], o);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        if (cur[m] >= 0) {
+                            if (lane == cur[m]) {
+                                ck[m] = gam[m] * kk[m];
+                                cq[m] = gam[m] * kq[m];
+                            }
+                            gam[m] *= dec_s[cur[m]];
+                            cur[m] = par[cur[m]];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int t = tw + 4 * m;
+                    if (t < lc) {
+                        if (lane < kSeg) {
+                            cks[t * kSeg + lane] = ck[m];
+                            cqs[t * kSeg + lane] = cq[m];
+                        }
+                        if (lane == 0) gam_s[t] = gam[m];
+                    }
+                }
+            }
+            // v of this thread's row, loaded while the accumulators finish
+            float vreg[kSeg];
+#pragma unroll
+            for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? __ldg(a.xc + (n0 + t) * C + voff + row) : 0.0f;
+            team_sync(team);  // coefficients written by every warp of the team
+
+            // ---- E: per row, the nodes in order ------------------------------------
+            // warp-uniform: tcgen05.ld is warp-collective
+            const bool ready =
+                __all_sync(0xffffffffu, wait_or_abort(bars + B_ACCFULL + team, uint32_t(ut & 1), abort_flag));
+            if (ready) {
+                gdn::tc_fence_after_sync();
+                const uint32_t trow = tmem + TEAM_COLS * team + (uint32_t((warp & 3) * 32) << 16);
+                float dv[32], p1[32];
+                gdn::tmem_ld32(trow + 0, dv);
+                gdn::tmem_ld32(trow + 32, p1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+                gdn::tmem_ld32(trow + 64, p1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+                gdn::tmem_ld32(trow + 96, p1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+                gdn::tmem_ld32(trow + SMALL_COL, p1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+                gdn::tc_fence_before_sync();
+                mbar_arrive(bars + B_ACCEMPTY + team);  // the accumulators may be overwritten
+
+                float u[kSeg];
+#pragma unroll
+                for (int t = 0; t < kSeg; ++t) {
+                    u[t] = 0.f;
+                    if (t < lc) {
+                        const int64_t n = n0 + t;
+                        float sk = gam_s[t] * dv[t];
+                        float oq = gam_s[t] * dv[kSeg + t];
+#pragma unroll
+                        for (int j4 = 0; j4 < (t + 4) / 4; ++j4) {
+                            const float4 ckv = *reinterpret_cast<const float4 *>(cks + t * kSeg + 4 * j4);
+                            const float4 cqv = *reinterpret_cast<const float4 *>(cqs + t * kSeg + 4 * j4);
+                            if (4 * j4 + 0 < t) sk = fmaf(ckv.x, u[4 * j4 + 0], sk);
+                            if (4 * j4 + 1 < t) sk = fmaf(ckv.y, u[4 * j4 + 1], sk);
+                            if (4 * j4 + 2 < t) sk = fmaf(ckv.z, u[4 * j4 + 2], sk);
+                            if (4 * j4 + 3 < t) sk = fmaf(ckv.w, u[4 * j4 + 3], sk);
+                            if (4 * j4 + 0 < t) oq = fmaf(cqv.x, u[4 * j4 + 0], oq);
+                            if (4 * j4 + 1 < t) oq = fmaf(cqv.y, u[4 * j4 + 1], oq);
+                            if (4 * j4 + 2 < t) oq = fmaf(cqv.z, u[4 * j4 + 2], oq);
+                            if (4 * j4 + 3 < t) oq = fmaf(cqv.w, u[4 * j4 + 3], oq);
+                        }
+                        u[t] = beta_s[t] * (vreg[t] - sk);
+                        oq = fmaf(cqs[t * kSeg + t], u[t], oq);
+                        a.o[(n * a.Hv + h) * D + row] = a.q_scale * oq;
+                        a.replay[(n * a.Hv + h) * a.rstride + D + row] = u[t];
+                    }
+                }
+            }
+            // after a timeout the team keeps looping (every wait now returns at
+            // once) so that all four warps meet at each team barrier
+        }
+    }
+
+    // ---- tear-down -------------------------------------------------------------
+    if (*abort_flag) {
         if (tid == 0) {
             gdn::record_status(a.status, GDN_DEV_TIMEOUT);
-            gdn::mbar_wait_bounded(full + 0, 0);
-            gdn::mbar_wait_bounded(full + 1, 0);
-            gdn::mbar_wait_bounded(mmab + 0, 0);
-            gdn::mbar_wait_bounded(mmab + 1, 0);
+            // drain whatever may still be in flight (bounded) before release
+            for (int kb = 0; kb < 4; ++kb) gdn::mbar_wait_bounded(bars + B_EMPTY + kb, uint32_t((nv - 1) & 1));
         }
     }
     gdn::tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         gdn::tc_fence_after_sync();
         gdn::tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -758,12 +862,23 @@ int launch(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
-    auto k = tree_verify_tc_kernel;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tcv::BYTES)) != cudaSuccess)
+    auto k = tree_verify_ws_kernel;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(wsv::BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    const dim3 grid{unsigned(a.Hv), unsigned(a.S)};
-    k<<<grid, kThreads, tcv::BYTES, st>>>(map, a);
+    const int64_t items = int64_t(a.S) * a.Hv;
+    const int sms = sm_count();
+    if (sms <= 0) return GDN_ERR_LAUNCH;
+    // one CTA per SM, each with at most kMaxItems items (more CTAs queue behind)
+    int64_t grid = std::max<int64_t>(std::min<int64_t>(items, sms), (items + wsv::kMaxItems - 1) / wsv::kMaxItems);
+    k<<<unsigned(grid), wsv::kThreadsWS, wsv::BYTES, st>>>(map, a);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
