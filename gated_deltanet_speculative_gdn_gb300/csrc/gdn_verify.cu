@@ -425,8 +425,9 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
 // work of different items overlap.
 namespace wsv {
 constexpr int D = 128;
-constexpr int kWarps = 10;
+constexpr int kWarps = 11;                       // producer, 2 MMA issuers, 2 teams of 4
 constexpr int kThreadsWS = kWarps * 32;
+constexpr int kTeam0 = 3;                        // first warp of team 0
 constexpr int kMaxItems = 64;                    // items per CTA
 constexpr uint32_t kChunk = 128 * 128;           // bytes of one S0 K-chunk
 constexpr uint32_t kBChunk = 32 * 128;           // bytes of one B K-chunk
@@ -435,24 +436,29 @@ constexpr uint32_t RAW = 0;                      // 4 ring slots: S0 chunk, hi i
 constexpr uint32_t LO = RAW + 4 * kChunk;        // 4 ring slots: lo of the chunk
 constexpr uint32_t BHI = LO + 4 * kChunk;        // per team
 constexpr uint32_t BLO = BHI + 2 * kBTeam;       // per team
-constexpr uint32_t SMALL = BLO + 2 * kBTeam;
+// q/k rows of the next item, as TMA boxes of [16 rows][32 floats]: k boxes
+// 0..3 (columns 32 b..), then q boxes 0..3
+constexpr uint32_t STAGE = BLO + 2 * kBTeam;
+constexpr uint32_t kStageBox = 16 * 32 * 4;
+constexpr uint32_t SMALL = STAGE + 32 * D * 4;
 // per-team small area (4-byte words)
 constexpr int T_CK = 0, T_CQ = 256, T_BETA = 512, T_DEC = 528, T_GAM = 544, T_PAR = 560, T_WORDS = 576;
-// CTA-wide words after the two team areas
-constexpr int W_BARS = 2 * T_WORDS;              // 22 mbarriers (8 B each)
-constexpr int W_TMEM = W_BARS + 44;
+// barriers: per team t: FULL 4 t + kb, SPLIT 8 + 4 t + kb, BREADY 16 + t, ACCFULL 18 + t,
+// ACCEMPTY 20 + t, SFULL 22 + t; shared: EMPTY 24 + kb, SEMPTY 28
+constexpr int B_FULL = 0, B_SPLIT = 8, B_BREADY = 16, B_ACCFULL = 18, B_ACCEMPTY = 20, B_SFULL = 22,
+              B_EMPTY = 24, B_SEMPTY = 28, N_BARS = 29;
+constexpr int W_BARS = 2 * T_WORDS;              // N_BARS mbarriers (8 B each)
+constexpr int W_TMEM = W_BARS + 2 * 32;
 constexpr int W_ABORT = W_TMEM + 1;
 constexpr int W_NV = W_ABORT + 1;
 constexpr int W_LIST = W_NV + 2;                 // kMaxItems x int4 (item, n0, ns, slot), 16-B aligned
 constexpr int SMALL_WORDS = W_LIST + 4 * kMaxItems;
 constexpr size_t BYTES = SMALL + SMALL_WORDS * 4 + 1024;
-// barrier indices
-// B_FULL + 4 t + kb: chunk kb of team t's current item landed (a team sees
-// every phase of its own barriers, never the other team's)
-constexpr int B_FULL = 0, B_SPLIT = 8, B_EMPTY = 12, B_BREADY = 16, B_ACCFULL = 18, B_ACCEMPTY = 20, N_BARS = 22;
 constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-// team t: columns 256 t + 32 kb (A_hi B_hi of chunk kb) and 256 t + 128 (small terms)
-constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256, SMALL_COL = 128;
+// team t, K-chunk kb: columns 256 t + 64 kb (A_hi B_hi) and 256 t + 64 kb + 32
+// (A_hi B_lo + A_lo B_hi).  Eight independent accumulation chains per item: the
+// tensor pipe overlaps them, and each truncating accumulation is short.
+constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256;
 
 __device__ __forceinline__ uint32_t sw_off(int row, int k, uint32_t chunk) {
     return uint32_t(k >> 5) * chunk + uint32_t(row) * 128u + ((uint32_t(((k & 31) >> 2) ^ (row & 7))) << 4) +
@@ -478,7 +484,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 }  // namespace wsv
 
 __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
-    tree_verify_ws_kernel(const __grid_constant__ CUtensorMap tmap, const VerifyArgs a) {
+    tree_verify_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap xmap,
+                          const VerifyArgs a) {
     using namespace wsv;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sb =
@@ -492,6 +499,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int total = a.S * a.Hv;
+    const int64_t C = a.C;
 
     // ---- set-up: this CTA's valid items, barriers, tensor memory -------------
     if (warp == 0) {
@@ -521,10 +529,9 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     }
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
-            const bool by_team = (i >= B_SPLIT && i < B_EMPTY) || (i >= B_BREADY && i < B_ACCFULL) ||
-                                 i >= B_ACCEMPTY;
-            const uint32_t cnt = by_team ? 128u : 1u;
-            gdn::mbar_init(bars + i, cnt);
+            const bool by_team = (i >= B_SPLIT && i < B_BREADY + 2) || (i >= B_ACCEMPTY && i < B_ACCEMPTY + 2) ||
+                                 i == B_SEMPTY;
+            gdn::mbar_init(bars + i, by_team ? 128u : 1u);
         }
         gdn::fence_mbar_init();
         *abort_flag = 0;
@@ -540,31 +547,47 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     const int nv = words[W_NV];
 
     if (warp == 0) {
-        // ---- producer: four S0 chunks per item into ring slots 0..3 -----------
+        // ---- producer: per item, its q/k rows into the stage, then its four
+        //      S0 chunks into ring slots 0..3 ------------------------------------
         if (lane == 0) {
             for (int v = 0; v < nv; ++v) {
                 const int4 e = list[v];
-                const int y = (e.w * a.Hv + e.x % a.Hv) * D;
+                const int h = e.x % a.Hv, kh = h / (a.Hv / a.Hk), n0 = e.y, lc = e.z;
+                const int t = v & 1;
+                if (v > 0 && !wait_or_abort(bars + B_SEMPTY, uint32_t((v - 1) & 1), abort_flag)) break;
+                // rows n0 .. n0 + 15 (rows past the last node are another sequence's
+                // or zero-filled past the tensor; the team ignores them)
+                gdn::mbar_arrive_expect_tx(bars + B_SFULL + t, 8 * kStageBox);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    gdn::tma_load_2d(sb + STAGE + b * kStageBox, &xmap, a.Hk * D + kh * D + 32 * b, n0,
+                                     bars + B_SFULL + t);  // k
+                    gdn::tma_load_2d(sb + STAGE + (4 + b) * kStageBox, &xmap, kh * D + 32 * b, n0,
+                                     bars + B_SFULL + t);  // q
+                }
+                (void)lc;
+                const int y = (e.w * a.Hv + h) * D;
                 for (int kb = 0; kb < 4; ++kb) {
                     if (v > 0 && !wait_or_abort(bars + B_EMPTY + kb, uint32_t((v - 1) & 1), abort_flag)) break;
-                    uint64_t *fb = bars + B_FULL + 4 * (v & 1) + kb;
+                    uint64_t *fb = bars + B_FULL + 4 * t + kb;
                     gdn::mbar_arrive_expect_tx(fb, kChunk);
                     gdn::tma_load_2d(sb + RAW + kb * kChunk, &tmap, 32 * kb, y, fb);
                 }
                 if (*abort_flag) break;
             }
         }
-    } else if (warp == 1) {
-        // ---- MMA issuer --------------------------------------------------------
+    } else if (warp == 1 || warp == 2) {
+        // ---- MMA issuer of team (warp - 1) -----------------------------------------
+        const int t = warp - 1;
         if (lane == 0) {
-            for (int v = 0; v < nv; ++v) {
-                const int t = v & 1, ut = v >> 1;
+            for (int v = t; v < nv; v += 2) {
+                const int ut = v >> 1;
                 if (!wait_or_abort(bars + B_BREADY + t, uint32_t(ut & 1), abort_flag)) break;
                 if (ut > 0 && !wait_or_abort(bars + B_ACCEMPTY + t, uint32_t((ut - 1) & 1), abort_flag)) break;
                 const uint32_t dacc = tmem + TEAM_COLS * t;
                 bool ok = true;
                 for (int kb = 0; kb < 4 && ok; ++kb) {
-                    if (!wait_or_abort(bars + B_SPLIT + kb, uint32_t(v & 1), abort_flag)) {
+                    if (!wait_or_abort(bars + B_SPLIT + 4 * t + kb, uint32_t(ut & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -573,11 +596,12 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                     uint64_t alo = gdn::desc_sw128(sbase + LO + kb * kChunk);
                     uint64_t bhi = gdn::desc_sw128(sbase + BHI + t * kBTeam + kb * kBChunk);
                     uint64_t blo = gdn::desc_sw128(sbase + BLO + t * kBTeam + kb * kBChunk);
+                    // a K-step of 8 tf32 is 32 bytes: 2 in the descriptors' address field
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks, ahi += 2, alo += 2, bhi += 2, blo += 2) {
-                        gdn::mma_tf32(dacc + 32u * kb, ahi, bhi, IDESC, ks != 0);
-                        gdn::mma_tf32(dacc + SMALL_COL, ahi, blo, IDESC, (kb | ks) != 0);
-                        gdn::mma_tf32(dacc + SMALL_COL, alo, bhi, IDESC, 1);
+                        gdn::mma_tf32(dacc + 64u * kb, ahi, bhi, IDESC, ks != 0);
+                        gdn::mma_tf32(dacc + 64u * kb + 32u, ahi, blo, IDESC, ks != 0);
+                        gdn::mma_tf32(dacc + 64u * kb + 32u, alo, bhi, IDESC, 1);
                     }
                     gdn::mma_commit(bars + B_EMPTY + kb);
                 }
@@ -587,29 +611,49 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         }
     } else {
         // ---- math teams ----------------------------------------------------------
-        const int team = (warp - 2) >> 2, tw = (warp - 2) & 3;   // warp within the team
-        const int ttid = tw * 32 + lane;                          // 0..127
-        const int row = (warp & 3) * 32 + lane;                   // tensor-memory lane = state row
+        const int team = (warp - kTeam0) >> 2, tw = (warp - kTeam0) & 3;  // warp within the team
+        const int ttid = tw * 32 + lane;                                   // 0..127
+        const int row = (warp & 3) * 32 + lane;                            // tensor-memory lane = state row
         int *tws = words + team * T_WORDS;
         float *cks = reinterpret_cast<float *>(tws + T_CK), *cqs = reinterpret_cast<float *>(tws + T_CQ);
         float *beta_s = reinterpret_cast<float *>(tws + T_BETA), *dec_s = reinterpret_cast<float *>(tws + T_DEC);
         float *gam_s = reinterpret_cast<float *>(tws + T_GAM);
         int *par = tws + T_PAR;
         unsigned char *bhi_t = sb + BHI + team * kBTeam, *blo_t = sb + BLO + team * kBTeam;
-        const int64_t C = a.C;
 
         for (int v = team; v < nv; v += 2) {
             const int ut = v >> 1;
             const int4 e = list[v];
-            const int s = e.x / a.Hv, h = e.x % a.Hv, n0 = e.y, lc = e.z;
-            const int kh = h / (a.Hv / a.Hk);
-            const int qoff = kh * D, koff = a.Hk * D + kh * D, voff = 2 * a.Hk * D + h * D;
-            (void)s;
+            const int h = e.x % a.Hv, n0 = e.y, lc = e.z;
+            const int voff = 2 * a.Hk * D + h * D;
             // the team's previous epilogue has finished reading the small area
             team_sync(team);
             // ---- A: parents, gates, normalised q and k into B (hi / lo) ----------
+            int p = -1;
+            if (ttid < lc) p = a.parents[n0 + ttid];
+            float bv = 0.f, av = 0.f, dtb = 0.f, Ah = 0.f;
+            if (tw == 0 && lane < lc) {
+                const int64_t n = n0 + lane;
+                bv = __ldg(a.ba + n * a.ba_stride + h);
+                av = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
+                dtb = __ldg(a.dt_bias + h);
+                Ah = __ldg(a.A + h);
+            }
+            // warp tw normalises B rows c = tw + 4 j: k^ of nodes tw + 4 j (j < 4)
+            // and q^ of the same nodes (j >= 4); lane l holds elements 4l..4l+3.
+            // The rows come from the stage the producer filled.
+            const bool staged = wait_or_abort(bars + B_SFULL + team, uint32_t(ut & 1), abort_flag);
+            float4 nvv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = tw + 4 * j, t = c & 15;
+                nvv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (staged && t < lc)
+                    nvv[j] = *reinterpret_cast<const float4 *>(sb + STAGE + ((c >> 4) * 4 + (lane >> 3)) * kStageBox +
+                                                               t * 128 + (lane & 7) * 16);
+            }
+            mbar_arrive(bars + B_SEMPTY);  // the stage may be refilled
             if (ttid < lc) {
-                int p = a.parents[n0 + ttid];
                 if (p < -1 || p >= ttid) {
                     gdn::record_status(a.status, GDN_DEV_BAD_PARENT);
                     p = -1;  // outputs of a failed call are unspecified; keep the walk in bounds
@@ -618,23 +662,10 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             }
             if (tw == 0 && lane < lc) {
                 const int64_t n = n0 + lane;
-                const float bv = __ldg(a.ba + n * a.ba_stride + h);
-                const float av = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
-                const float dec = expf(gdn::softplus_f(av + a.dt_bias[h]) * a.A[h]);
+                const float dec = expf(gdn::softplus_f(av + dtb) * Ah);
                 beta_s[lane] = gdn::sigmoid_f(bv);
                 dec_s[lane] = dec;
                 a.replay[(n * a.Hv + h) * a.rstride + 2 * D] = dec;
-            }
-            // warp tw normalises B rows c = tw + 4 j: k^ of nodes tw + 4 j (j < 4)
-            // and q^ of the same nodes (j >= 4); lane l holds elements 4l..4l+3
-            float4 nvv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = tw + 4 * j, t = c & 15;
-                nvv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < lc)
-                    nvv[j] = __ldg(reinterpret_cast<const float4 *>(a.xc + (n0 + t) * C + (c < kSeg ? koff : qoff) +
-                                                                    4 * lane));
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -674,7 +705,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                     lo[f] = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
                 }
                 gdn::fence_proxy_async_smem();
-                mbar_arrive(bars + B_SPLIT + kb);
+                mbar_arrive(bars + B_SPLIT + 4 * team + kb);
             }
             team_sync(team);  // parents and decays written by other warps of the team
 
@@ -756,20 +787,15 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             if (ready) {
                 gdn::tc_fence_after_sync();
                 const uint32_t trow = tmem + TEAM_COLS * team + (uint32_t((warp & 3) * 32) << 16);
+                // D = sum over the 8 partial accumulators, added in fp32
                 float dv[32], p1[32];
                 gdn::tmem_ld32(trow + 0, dv);
-                gdn::tmem_ld32(trow + 32, p1);
+#pragma unroll 1
+                for (int part = 1; part < 8; ++part) {
+                    gdn::tmem_ld32(trow + 32u * part, p1);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
-                gdn::tmem_ld32(trow + 64, p1);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
-                gdn::tmem_ld32(trow + 96, p1);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
-                gdn::tmem_ld32(trow + SMALL_COL, p1);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+                    for (int i = 0; i < 32; ++i) dv[i] += p1[i];
+                }
                 gdn::tc_fence_before_sync();
                 mbar_arrive(bars + B_ACCEMPTY + team);  // the accumulators may be overwritten
 
@@ -869,7 +895,24 @@ int sm_count() {
     return n;
 }
 
+// xc viewed as [N rows][C floats]; boxes of [16 rows][32 floats] (the q or k
+// rows of one sequence's 16 nodes, 32 columns at a time)
+int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return GDN_ERR_TMA;
+    cuuint64_t gdim[2] = {cuuint64_t(C), cuuint64_t(N)};
+    cuuint64_t gstride[1] = {cuuint64_t(C) * 4};
+    cuuint32_t box[2] = {32, 16};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(xc), gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
+}
+
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
+    CUtensorMap xmap;
+    if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C)) return rc;
     auto k = tree_verify_ws_kernel;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(wsv::BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
@@ -878,7 +921,7 @@ int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     if (sms <= 0) return GDN_ERR_LAUNCH;
     // one CTA per SM, each with at most kMaxItems items (more CTAs queue behind)
     int64_t grid = std::max<int64_t>(std::min<int64_t>(items, sms), (items + wsv::kMaxItems - 1) / wsv::kMaxItems);
-    k<<<unsigned(grid), wsv::kThreadsWS, wsv::BYTES, st>>>(map, a);
+    k<<<unsigned(grid), wsv::kThreadsWS, wsv::BYTES, st>>>(map, xmap, a);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
