@@ -399,73 +399,113 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
 // warp-specialised pipeline.
 //
 // Per (sequence, value head) "item" the contraction
-//     D[i][c] = sum_k S0[i][k] B[c][k],   B = [k^_0..k^_15 | q^_0..q^_15] (unscaled)
-// is a 128 x 32 x 128 matrix product.  It runs on tcgen05 with accumulators in
-// tensor memory, as three tf32 products that recover fp32 accuracy (x = hi +
-// lo, hi = x with the low 13 mantissa bits cleared, lo exact):
-//     D = A_hi B_hi + A_hi B_lo + A_lo B_hi      (the dropped A_lo B_lo ~ 2^-22)
-// The tensor cores align and truncate when they accumulate, so the A_hi B_hi
-// term of each K-chunk gets an accumulator of its own and the two small terms
-// share one; the epilogue adds them in fp32.
+//     D[i][c] = sum_k S0[i][k] B[c][k],   B = [k_0..k_15 | q_0..q_15]   (raw rows)
+// is a 128 x 32 x 128 matrix product on tcgen05 with accumulators in tensor
+// memory, split so that it keeps fp32 accuracy (x = hi + lo, hi = x with the
+// low 13 mantissa bits cleared, lo exact):
+//     D = A_hi [B_hi | B_lo] + A_lo B_hi      (the dropped A_lo B_lo ~ 2^-22)
+// The first term is one tf32 product with N = 64 (B_hi and B_lo stacked).
+// The second, ~2^-11 of D, runs in fp16 (K = 16 per instruction) on 2^10 A_lo
+// (clear of fp16 subnormals), which costs it ~2^-12 of its own size; bf16's
+// 2^-9 is not enough, since the recurrence amplifies errors in S0 k.  A
+// tensor-core instruction takes about the same time for any N up to 256, so
+// this needs 24 instructions per item where three N = 32 tf32 products would
+// need 48.  The tensor cores read an fp32 operand as its hi part, so S0 and B
+// feed the hi operands unchanged.  The tensor cores align and truncate when
+// they accumulate, so the terms get short accumulators of their own, added in
+// fp32 by the epilogue.
+//
+// B holds the raw q/k rows, so the products start as soon as they land; the
+// epilogue scales column c by 1/|k_c| or 1/|q_c| (folded into Gamma_t), which
+// equals S0 k^ up to rounding.  The Gram terms of B with itself (k . k, q . k
+// and the norms) come from the tensor cores as well: 16 more tf32 products
+// (M = N = 64, B's rows [k | q | k_lo | q_lo] against themselves, so hi x hi,
+// hi x lo and lo x hi all appear).  The path coefficients then take a walk up
+// each node's ancestors that multiplies the decays.
 //
 // One CTA per SM walks a list of items.  Warp roles:
-//   warp 0       TMA producer: streams each item's S0 as four 16 KB K-chunks
+//   warp 0       TMA producer: S0 of each item as four 16 KB K-chunks
 //                ([128 rows][32 floats], 128-byte swizzle = the tensor cores'
-//                K-major operand layout) into a four-slot ring;
-//   warp 1       MMA issuer: once a chunk is split and the item's B is ready,
-//                issues the chunk's 12 MMAs into the item's team accumulators;
-//   warps 2-5    team 0 and warps 6-9 team 1, on alternate items: q/k/v and
-//                gates, B = normalised q/k split into hi/lo, the split of each
-//                S0 chunk (hi in place, lo beside it), the path coefficients
-//                (dot products along each node's ancestors, shuffle-reduced),
-//                and the per-row epilogue reading the accumulators from tensor
-//                memory (thread i owns state row i).
-// While one team runs an item's epilogue the other prepares the next item and
-// the producer keeps the ring full, so loads, tensor-core work and CUDA-core
-// work of different items overlap.
+//                K-major operand layout) into a six-slot ring;
+//   warp 1       MMA issuer: per item, the Gram terms once its B is in; per
+//                chunk, A_hi [B_hi | B_lo] once the chunk lands, A_lo B_hi
+//                once its lo part is out;
+//   warps 2-3    splitters, items in order: B's lo part and fp16 copy as soon
+//                as the item's q/k rows land, then the lo part of every S0
+//                chunk as fp16 into a ring of two-chunk tiles, so S0 slots turn
+//                over at load speed;
+//   warps 4-7    team 0 and warps 8-11 team 1, on alternate items: the item's
+//                q/k rows by TMA into the team's B buffer (same layout as the
+//                chunks), gates, norms and path coefficients from the Gram
+//                terms, and the per-row epilogue reading the accumulators from
+//                tensor memory (thread i owns state row i).
+// A team's next q/k rows (loaded by the team) land while it runs the current
+// epilogue, and the S0 ring runs ahead of both teams, so loads, tensor-core
+// work and CUDA-core work of different items overlap.
 namespace wsv {
 constexpr int D = 128;
-constexpr int kWarps = 11;                       // producer, 2 MMA issuers, 2 teams of 4
+constexpr int kWarps = 12;
 constexpr int kThreadsWS = kWarps * 32;
-constexpr int kTeam0 = 3;                        // first warp of team 0
-constexpr int kMaxItems = 64;                    // items per CTA
-constexpr uint32_t kChunk = 128 * 128;           // bytes of one S0 K-chunk
-constexpr uint32_t kBChunk = 32 * 128;           // bytes of one B K-chunk
-constexpr uint32_t kBTeam = 4 * kBChunk;         // one team's B (hi or lo)
-constexpr uint32_t RAW = 0;                      // 4 ring slots: S0 chunk, hi in place
-constexpr uint32_t LO = RAW + 4 * kChunk;        // 4 ring slots: lo of the chunk
-constexpr uint32_t BHI = LO + 4 * kChunk;        // per team
-constexpr uint32_t BLO = BHI + 2 * kBTeam;       // per team
-// q/k rows of the next item, as TMA boxes of [16 rows][32 floats]: k boxes
-// 0..3 (columns 32 b..), then q boxes 0..3
-constexpr uint32_t STAGE = BLO + 2 * kBTeam;
-constexpr uint32_t kStageBox = 16 * 32 * 4;
-constexpr uint32_t SMALL = STAGE + 32 * D * 4;
-// per-team small area (4-byte words)
-constexpr int T_CK = 0, T_CQ = 256, T_BETA = 512, T_DEC = 528, T_GAM = 544, T_PAR = 560, T_WORDS = 576;
-// barriers: per team t: FULL 4 t + kb, SPLIT 8 + 4 t + kb, BREADY 16 + t, ACCFULL 18 + t,
-// ACCEMPTY 20 + t, SFULL 22 + t; shared: EMPTY 24 + kb, SEMPTY 28
-constexpr int B_FULL = 0, B_SPLIT = 8, B_BREADY = 16, B_ACCFULL = 18, B_ACCEMPTY = 20, B_SFULL = 22,
-              B_EMPTY = 24, B_SEMPTY = 28, N_BARS = 29;
-constexpr int W_BARS = 2 * T_WORDS;              // N_BARS mbarriers (8 B each)
-constexpr int W_TMEM = W_BARS + 2 * 32;
+constexpr int kSplit0 = 2, kSplitThreads = 64;     // splitter warps 2-3
+constexpr int kTeam0 = 4;                          // team t: warps 4 + 4t .. 7 + 4t
+constexpr int kMaxItems = 64;                      // items per CTA
+constexpr int NR = 6;                              // S0 ring depth (K-chunks)
+constexpr int NLP = 2;                             // lo ring depth (two-chunk fp16 tiles)
+constexpr uint32_t kChunk = 128 * 128;             // one S0 K-chunk: 128 rows x 32 fp32
+constexpr uint32_t kLoTile = 128 * 128;            // S0 lo of two K-chunks: 128 rows x 64 fp16
+constexpr uint32_t kBChunk = 64 * 128;             // one B K-chunk: rows 0-31 hi, 32-63 lo (fp32)
+constexpr uint32_t kBTeam = 4 * kBChunk;           // one team's tf32 B
+constexpr uint32_t kBHTile = 32 * 128;             // fp16 B of two K-chunks: 32 rows x 64 fp16
+constexpr uint32_t kBHTeam = 2 * kBHTile;          // one team's fp16 B
+constexpr uint32_t kQKBox = 16 * 128;              // 16 rows of k or q, one K-chunk
+constexpr uint32_t RAW = 0;
+constexpr uint32_t LO = RAW + NR * kChunk;
+constexpr uint32_t BT = LO + NLP * kLoTile;        // per team: q/k rows normalised in place, lo below
+constexpr uint32_t BH = BT + 2 * kBTeam;           // per team
+constexpr uint32_t SMALL = BH + 2 * kBHTeam;
+// per-team small area (4-byte words): the Gram terms as partial sums from the
+// four tensor-memory lane quarters, KA + KB = k_t . k_j and QA + QB = q_t . k_j
+// ([16][16]; the path coefficients ck, cq then overwrite KA, QA in place),
+// QQA + QQB = q_t . q_t, gates, parents, gsk, gsq = Gamma_t / |k_t|, Gamma_t / |q_t|
+constexpr int T_KA = 0, T_KB = 256, T_QA = 512, T_QB = 768, T_BETA = 1024, T_DEC = 1040, T_GSK = 1056,
+              T_PAR = 1072, T_GSQ = 1088, T_QQA = 1104, T_QQB = 1120, T_WORDS = 1136;
+// mbarriers
+constexpr int B_RFULL = 0;                 // NR: S0 chunk landed
+constexpr int B_REMPTY = B_RFULL + NR;     // NR: chunk split and its A_hi products done (64 + 1 arrivals)
+constexpr int B_LFULL = B_REMPTY + NR;     // 2 NLP, one per chunk half: lo part written (64)
+constexpr int B_LEMPTY = B_LFULL + 2 * NLP;  // NLP: the tile's A_lo products done (1)
+constexpr int B_QFULL = B_LEMPTY + NLP;    // per team: q/k rows landed (1 + bytes)
+constexpr int B_BREADY = B_QFULL + 2;      // per team: B split into lo and fp16 parts (64)
+constexpr int B_GFULL = B_BREADY + 2;      // per team: Gram terms complete (1)
+constexpr int B_ACCFULL = B_GFULL + 2;     // per team: accumulators complete (1)
+constexpr int B_ACCEMPTY = B_ACCFULL + 2;  // per team: accumulators read (128)
+constexpr int B_DRAIN = B_ACCEMPTY + 2;    // the issuer's last tensor-core work done (1)
+constexpr int N_BARS = B_DRAIN + 1;
+constexpr int W_BARS = 2 * T_WORDS;
+constexpr int W_TMEM = W_BARS + 2 * N_BARS;
 constexpr int W_ABORT = W_TMEM + 1;
 constexpr int W_NV = W_ABORT + 1;
-constexpr int W_LIST = W_NV + 2;                 // kMaxItems x int4 (item, n0, ns, slot), 16-B aligned
+constexpr int W_LIST = (W_NV + 4) & ~3;            // kMaxItems x int4 (item, n0, ns, slot), 16-B aligned
 constexpr int SMALL_WORDS = W_LIST + 4 * kMaxItems;
 constexpr size_t BYTES = SMALL + SMALL_WORDS * 4 + 1024;
-constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-// team t, K-chunk kb: columns 256 t + 64 kb (A_hi B_hi) and 256 t + 64 kb + 32
-// (A_hi B_lo + A_lo B_hi).  Eight independent accumulation chains per item: the
-// tensor pipe overlaps them, and each truncating accumulation is short.
-constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256;
+static_assert(BYTES <= 227 * 1024, "shared memory");
+static_assert((W_BARS % 2) == 0, "mbarriers are 8-byte aligned");
+// instruction descriptors: fp32 accumulate, K-major operands, M = 128;
+// tf32 x tf32 with N = 64 and fp16 x fp16 with N = 32
+constexpr uint32_t IDESC_TF32 = (1u << 4) | (2u << 7) | (2u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t IDESC_F16 = (1u << 4) | (0u << 7) | (0u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+// the Gram terms: tf32, M = 64, N = 64, both operands the team's stacked B
+constexpr uint32_t IDESC_GRAM = (1u << 4) | (2u << 7) | (2u << 10) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
+constexpr float kLoScale = 1024.0f;                // A_lo is stored as fp16(2^10 A_lo)
+// Team t's accumulators start at column 256 t: K-half kh (chunks 2 kh, 2 kh + 1)
+// owns columns 64 kh .. 64 kh + 63, A_hi B_hi in the first 32 and A_hi B_lo in
+// the last 32; 2^10 A_lo B_hi of all four K-chunks sits at 128.  The Gram terms
+// G = B B^T (M = 64: row a of G in lane 32 (a / 16) + a % 16) sit at 192.
+constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256, LHCOL = 128, GCOL = 192;
 
 __device__ __forceinline__ uint32_t sw_off(int row, int k, uint32_t chunk) {
     return uint32_t(k >> 5) * chunk + uint32_t(row) * 128u + ((uint32_t(((k & 31) >> 2) ^ (row & 7))) << 4) +
            uint32_t(k & 3) * 4u;
-}
-__device__ __forceinline__ float4 add4(float4 a, float4 b) {
-    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 __device__ __forceinline__ void team_sync(int team) {
     asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(128) : "memory");
@@ -480,6 +520,21 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gdn::smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ float4 lo4(float4 x) {
+    return make_float4(x.x - gdn::tf32_hi(x.x), x.y - gdn::tf32_hi(x.y), x.z - gdn::tf32_hi(x.z),
+                       x.w - gdn::tf32_hi(x.w));
+}
+// -(x with the low 13 mantissa bits cleared)
+__device__ __forceinline__ float neg_hi(float x) { return __uint_as_float((__float_as_uint(x) & 0xFFFFE000u) ^ 0x80000000u); }
+__device__ __forceinline__ uint2 f16x4(float4 x) {
+    return make_uint2(gdn::pack_f16x2(x.x, x.y), gdn::pack_f16x2(x.z, x.w));
+}
+// Byte offset of 16-bit elements k..k+3 (k % 4 == 0) of row `row` in a K-major
+// operand of 64 elements per row in the 128-byte swizzle (tile k >> 6).
+__device__ __forceinline__ uint32_t sw_off_h(int row, int k, uint32_t tile) {
+    return uint32_t(k >> 6) * tile + uint32_t(row) * 128u + ((uint32_t(((k & 63) >> 3) ^ (row & 7))) << 4) +
+           uint32_t((k >> 2) & 1) * 8u;
 }
 }  // namespace wsv
 
@@ -529,9 +584,12 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     }
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
-            const bool by_team = (i >= B_SPLIT && i < B_BREADY + 2) || (i >= B_ACCEMPTY && i < B_ACCEMPTY + 2) ||
-                                 i == B_SEMPTY;
-            gdn::mbar_init(bars + i, by_team ? 128u : 1u);
+            uint32_t count = 1;
+            if (i >= B_REMPTY && i < B_REMPTY + NR) count = kSplitThreads + 1;
+            if (i >= B_LFULL && i < B_LFULL + 2 * NLP) count = kSplitThreads;
+            if (i >= B_BREADY && i < B_BREADY + 2) count = kSplitThreads;
+            if (i >= B_ACCEMPTY && i < B_ACCEMPTY + 2) count = 128;
+            gdn::mbar_init(bars + i, count);
         }
         gdn::fence_mbar_init();
         *abort_flag = 0;
@@ -545,118 +603,216 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     gdn::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int nv = words[W_NV];
+    const int nchunks = 4 * nv;
 
     if (warp == 0) {
-        // ---- producer: per item, its q/k rows into the stage, then its four
-        //      S0 chunks into ring slots 0..3 ------------------------------------
+        // ---- producer: S0 chunks in order into the ring ----------------------
         if (lane == 0) {
-            for (int v = 0; v < nv; ++v) {
-                const int4 e = list[v];
-                const int h = e.x % a.Hv, kh = h / (a.Hv / a.Hk), n0 = e.y, lc = e.z;
-                const int t = v & 1;
-                if (v > 0 && !wait_or_abort(bars + B_SEMPTY, uint32_t((v - 1) & 1), abort_flag)) break;
-                // rows n0 .. n0 + 15 (rows past the last node are another sequence's
-                // or zero-filled past the tensor; the team ignores them)
-                gdn::mbar_arrive_expect_tx(bars + B_SFULL + t, 8 * kStageBox);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    gdn::tma_load_2d(sb + STAGE + b * kStageBox, &xmap, a.Hk * D + kh * D + 32 * b, n0,
-                                     bars + B_SFULL + t);  // k
-                    gdn::tma_load_2d(sb + STAGE + (4 + b) * kStageBox, &xmap, kh * D + 32 * b, n0,
-                                     bars + B_SFULL + t);  // q
+            int g = 0;
+            for (; g < nchunks; ++g) {
+                const int r = g % NR;
+                if (g >= NR && !wait_or_abort(bars + B_REMPTY + r, uint32_t((g / NR - 1) & 1), abort_flag)) break;
+                const int4 e = list[g >> 2];
+                uint64_t *fb = bars + B_RFULL + r;
+                gdn::mbar_arrive_expect_tx(fb, kChunk);
+                gdn::tma_load_2d(sb + RAW + r * kChunk, &tmap, 32 * (g & 3), (e.w * a.Hv + e.x % a.Hv) * D, fb);
+            }
+            if (*abort_flag) {
+                // copies still in flight land on their own: wait for them (bounded)
+                for (int r = 0; r < NR; ++r) {
+                    const int last = g - 1 - ((g - 1 - r) % NR + NR) % NR;  // last chunk issued into slot r
+                    if (g > 0 && last >= 0) gdn::mbar_wait_bounded(bars + B_RFULL + r, uint32_t((last / NR) & 1));
                 }
-                (void)lc;
-                const int y = (e.w * a.Hv + h) * D;
-                for (int kb = 0; kb < 4; ++kb) {
-                    if (v > 0 && !wait_or_abort(bars + B_EMPTY + kb, uint32_t((v - 1) & 1), abort_flag)) break;
-                    uint64_t *fb = bars + B_FULL + 4 * t + kb;
-                    gdn::mbar_arrive_expect_tx(fb, kChunk);
-                    gdn::tma_load_2d(sb + RAW + kb * kChunk, &tmap, 32 * kb, y, fb);
-                }
-                if (*abort_flag) break;
             }
         }
-    } else if (warp == 1 || warp == 2) {
-        // ---- MMA issuer of team (warp - 1) -----------------------------------------
-        const int t = warp - 1;
+    } else if (warp == 1) {
+        // ---- MMA issuer: items and chunks in order -----------------------------
         if (lane == 0) {
-            for (int v = t; v < nv; v += 2) {
-                const int ut = v >> 1;
+            bool ok = true;
+            for (int v = 0; v < nv && ok; ++v) {
+                const int t = v & 1, ut = v >> 1;
                 if (!wait_or_abort(bars + B_BREADY + t, uint32_t(ut & 1), abort_flag)) break;
                 if (ut > 0 && !wait_or_abort(bars + B_ACCEMPTY + t, uint32_t((ut - 1) & 1), abort_flag)) break;
                 const uint32_t dacc = tmem + TEAM_COLS * t;
-                bool ok = true;
-                for (int kb = 0; kb < 4 && ok; ++kb) {
-                    if (!wait_or_abort(bars + B_SPLIT + 4 * t + kb, uint32_t(ut & 1), abort_flag)) {
+                const uint32_t bt0 = sbase + BT + t * kBTeam, bh0 = sbase + BH + t * kBHTeam;
+                // Gram terms of B's 64 rows [k | q | k_lo | q_lo] with themselves:
+                // hi x hi, hi x lo and lo x hi all appear in the one product
+                for (int kb = 0; kb < 4; ++kb) {
+                    uint64_t gd = gdn::desc_sw128(bt0 + kb * kBChunk);
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks, gd += 2)
+                        gdn::mma_tf32(dacc + GCOL, gd, gd, IDESC_GRAM, (kb | ks) != 0);
+                }
+                gdn::mma_commit(bars + B_GFULL + t);
+                for (int kb = 0; kb < 4; ++kb) {
+                    const int g = 4 * v + kb, r = g % NR, q = g % (2 * NLP), l = (g >> 1) % NLP;
+                    if (!wait_or_abort(bars + B_RFULL + r, uint32_t((g / NR) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
                     gdn::tc_fence_after_sync();
-                    uint64_t ahi = gdn::desc_sw128(sbase + RAW + kb * kChunk);
-                    uint64_t alo = gdn::desc_sw128(sbase + LO + kb * kChunk);
-                    uint64_t bhi = gdn::desc_sw128(sbase + BHI + t * kBTeam + kb * kBChunk);
-                    uint64_t blo = gdn::desc_sw128(sbase + BLO + t * kBTeam + kb * kBChunk);
-                    // a K-step of 8 tf32 is 32 bytes: 2 in the descriptors' address field
+                    const uint32_t dk = dacc + 64u * (kb >> 1);
+                    uint64_t ahi = gdn::desc_sw128(sbase + RAW + r * kChunk);
+                    uint64_t bst = gdn::desc_sw128(bt0 + kb * kBChunk);  // [B_hi | B_lo], 64 rows
+                    // a K-step (8 tf32 or 16 fp16) is 32 bytes: 2 in the descriptors' address field
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks, ahi += 2, alo += 2, bhi += 2, blo += 2) {
-                        gdn::mma_tf32(dacc + 64u * kb, ahi, bhi, IDESC, ks != 0);
-                        gdn::mma_tf32(dacc + 64u * kb + 32u, ahi, blo, IDESC, ks != 0);
-                        gdn::mma_tf32(dacc + 64u * kb + 32u, alo, bhi, IDESC, 1);
+                    for (int ks = 0; ks < 4; ++ks, ahi += 2, bst += 2)
+                        gdn::mma_tf32(dk, ahi, bst, IDESC_TF32, ((kb & 1) | ks) != 0);
+                    gdn::mma_commit(bars + B_REMPTY + r);
+                    if (!wait_or_abort(bars + B_LFULL + q, uint32_t((g / (2 * NLP)) & 1), abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    gdn::mma_commit(bars + B_EMPTY + kb);
+                    gdn::tc_fence_after_sync();
+                    // this chunk's 32 K-columns are the (kb & 1) half of the two-chunk tiles
+                    uint64_t alo = gdn::desc_sw128(sbase + LO + l * kLoTile + 64u * (kb & 1));
+                    uint64_t bh = gdn::desc_sw128(bh0 + (kb >> 1) * kBHTile + 64u * (kb & 1));
+#pragma unroll 1
+                    for (int ks = 0; ks < 2; ++ks, alo += 2, bh += 2)
+                        gdn::mma_f16(dacc + LHCOL, alo, bh, IDESC_F16, (kb | ks) != 0);
+                    if (g & 1) gdn::mma_commit(bars + B_LEMPTY + l);
                 }
-                if (!ok) break;
-                gdn::mma_commit(bars + B_ACCFULL + t);
+                if (ok) gdn::mma_commit(bars + B_ACCFULL + t);
+            }
+            // every tensor-core operation of this thread completes before the
+            // tensor memory is released
+            gdn::mma_commit(bars + B_DRAIN);
+            gdn::mbar_wait_bounded(bars + B_DRAIN, 0);
+        }
+    } else if (warp < kTeam0) {
+        // ---- splitters, items in order: the lo and fp16 parts of the item's raw
+        //      q/k rows (B), then 2^10 (x - hi) of each S0 chunk as fp16.  Chunk g
+        //      fills half g & 1 of lo tile (g / 2) % NLP. ----------------------------
+        const int st = tid - kSplit0 * 32;
+        // S0 chunks: thread st takes rows rg + 8 j (j < 16) at 16-byte unit u, which
+        // holds K-columns k .. k + 3 (the swizzle phase of those rows is rg).  A
+        // warp's four rows rg cover both bank halves of the fp16 tile.  The fp16
+        // lo goes to byte dst0 (first half of a tile) or dst1 (second half), plus
+        // 1024 j.
+        const int sl = st & 31, u = sl & 7;
+        const int rg = ((sl >> 3) & 1) | ((st >> 5) << 1) | (((sl >> 4) & 1) << 2);
+        const int k = 4 * (u ^ rg);
+        const uint32_t src = uint32_t(rg) * 128u + uint32_t(u) * 16u;
+        const uint32_t dst0 = uint32_t(rg) * 128u + (uint32_t((k >> 3) ^ rg) << 4) + uint32_t((k >> 2) & 1) * 8u;
+        const uint32_t dst1 = uint32_t(rg) * 128u + (uint32_t(((32 + k) >> 3) ^ rg) << 4) + uint32_t((k >> 2) & 1) * 8u;
+        const uint64_t scale = gdn::f2pack(kLoScale, kLoScale);
+        bool ok = true;
+        for (int v = 0; v < nv && ok; ++v) {
+            const int t = v & 1;
+            // B: rows c (k of node c, then q of node c - 16) of each K-chunk; lo
+            // below them (rows 32 + c, same swizzle phase), fp16 copy beside
+            if (!wait_or_abort(bars + B_QFULL + t, uint32_t((v >> 1) & 1), abort_flag)) break;
+            {
+                unsigned char *bt = sb + BT + t * kBTeam, *bh = sb + BH + t * kBHTeam;
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j) {
+                    const int kb = j >> 2, c = (st >> 3) + 8 * (j & 3), uu = st & 7;
+                    unsigned char *p = bt + kb * kBChunk + c * 128 + uu * 16;
+                    const float4 x = *reinterpret_cast<const float4 *>(p);
+                    *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
+                    *reinterpret_cast<uint2 *>(bh + sw_off_h(c, 32 * kb + 4 * (uu ^ (c & 7)), kBHTile)) = f16x4(x);
+                }
+                gdn::fence_proxy_async_smem();
+                mbar_arrive(bars + B_BREADY + t);
+            }
+            for (int kb = 0; kb < 4; ++kb) {
+                const int g = 4 * v + kb, r = g % NR, pi = g >> 1, l = pi % NLP;
+                if (!wait_or_abort(bars + B_RFULL + r, uint32_t((g / NR) & 1), abort_flag) ||
+                    (!(g & 1) && pi >= NLP &&
+                     !wait_or_abort(bars + B_LEMPTY + l, uint32_t((pi / NLP - 1) & 1), abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char *raw = sb + RAW + r * kChunk + src;
+                unsigned char *lo = sb + LO + l * kLoTile + ((g & 1) ? dst1 : dst0);
+                constexpr int kPer = int(kChunk / 16) / kSplitThreads;  // 16 float4 per thread, in two batches
+#pragma unroll
+                for (int b = 0; b < kPer; b += kPer / 2) {
+                    float4 x[kPer / 2];
+#pragma unroll
+                    for (int j = 0; j < kPer / 2; ++j) x[j] = *reinterpret_cast<const float4 *>(raw + 1024 * (b + j));
+#pragma unroll
+                    for (int j = 0; j < kPer / 2; ++j) {
+                        // 2^10 (x - hi): x plus hi with its sign flipped is exact, and so is the scaling
+                        const uint64_t lo01 = gdn::mul2(
+                            gdn::add2(gdn::f2pack(x[j].x, x[j].y), gdn::f2pack(neg_hi(x[j].x), neg_hi(x[j].y))), scale);
+                        const uint64_t lo23 = gdn::mul2(
+                            gdn::add2(gdn::f2pack(x[j].z, x[j].w), gdn::f2pack(neg_hi(x[j].z), neg_hi(x[j].w))), scale);
+                        const float2 fa = gdn::f2unpack(lo01), fb = gdn::f2unpack(lo23);
+                        *reinterpret_cast<uint2 *>(lo + 1024 * (b + j)) =
+                            make_uint2(gdn::pack_f16x2(fa.x, fa.y), gdn::pack_f16x2(fb.x, fb.y));
+                    }
+                }
+                gdn::fence_proxy_async_smem();
+                mbar_arrive(bars + B_REMPTY + r);
+                mbar_arrive(bars + B_LFULL + g % (2 * NLP));
             }
         }
     } else {
         // ---- math teams ----------------------------------------------------------
-        const int team = (warp - kTeam0) >> 2, tw = (warp - kTeam0) & 3;  // warp within the team
-        const int ttid = tw * 32 + lane;                                   // 0..127
-        const int row = (warp & 3) * 32 + lane;                            // tensor-memory lane = state row
+        const int team = (warp - kTeam0) >> 2, tw = warp & 3;  // warp within the team = its TMEM lane quarter
+        const int ttid = tw * 32 + lane;                       // 0..127
+        const int row = ttid;                                  // tensor-memory lane = state row
         int *tws = words + team * T_WORDS;
-        float *cks = reinterpret_cast<float *>(tws + T_CK), *cqs = reinterpret_cast<float *>(tws + T_CQ);
+        float *ka = reinterpret_cast<float *>(tws + T_KA), *kb = reinterpret_cast<float *>(tws + T_KB);
+        float *qa = reinterpret_cast<float *>(tws + T_QA), *qb = reinterpret_cast<float *>(tws + T_QB);
+        float *qqa = reinterpret_cast<float *>(tws + T_QQA), *qqb = reinterpret_cast<float *>(tws + T_QQB);
         float *beta_s = reinterpret_cast<float *>(tws + T_BETA), *dec_s = reinterpret_cast<float *>(tws + T_DEC);
-        float *gam_s = reinterpret_cast<float *>(tws + T_GAM);
+        float *gsk = reinterpret_cast<float *>(tws + T_GSK), *gsq = reinterpret_cast<float *>(tws + T_GSQ);
         int *par = tws + T_PAR;
-        unsigned char *bhi_t = sb + BHI + team * kBTeam, *blo_t = sb + BLO + team * kBTeam;
+        unsigned char *bt_t = sb + BT + team * kBTeam;
+
+        // parents and gate inputs of the team's next item, loaded one item ahead
+        int p_nx = -1;
+        float bv_nx = 0.f, av_nx = 0.f, dtb_nx = 0.f, ah_nx = 0.f;
+        auto prefetch = [&](int v) {
+            if (v >= nv) return;
+            const int4 e = list[v];
+            const int h = e.x % a.Hv, n0 = e.y, lc = e.z;
+            p_nx = ttid < lc ? __ldg(a.parents + n0 + ttid) : -1;
+            if (tw == 0 && lane < lc) {
+                const int64_t n = n0 + lane;
+                bv_nx = __ldg(a.ba + n * a.ba_stride + h);
+                av_nx = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
+                dtb_nx = __ldg(a.dt_bias + h);
+                ah_nx = __ldg(a.A + h);
+            }
+        };
+        prefetch(team);
+        // one thread of the team loads an item's raw q/k rows into the team's B
+        // (rows n0 .. n0 + 15; rows past the last node are another sequence's or
+        // zero-filled past the tensor, and the team zeroes them)
+        int qk_issued = 0;
+        auto issue_qk = [&](int v) {
+            if (ttid != 0 || v >= nv) return;
+            const int4 e = list[v];
+            const int h = e.x % a.Hv, kh = h / (a.Hv / a.Hk);
+            uint64_t *qb = bars + B_QFULL + team;
+            gdn::mbar_arrive_expect_tx(qb, 8 * kQKBox);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) {
+                gdn::tma_load_2d(bt_t + kb * kBChunk, &xmap, a.Hk * D + kh * D + 32 * kb, e.y, qb);
+                gdn::tma_load_2d(bt_t + kb * kBChunk + kQKBox, &xmap, kh * D + 32 * kb, e.y, qb);
+            }
+            ++qk_issued;
+        };
+        issue_qk(team);
 
         for (int v = team; v < nv; v += 2) {
             const int ut = v >> 1;
             const int4 e = list[v];
             const int h = e.x % a.Hv, n0 = e.y, lc = e.z;
             const int voff = 2 * a.Hk * D + h * D;
+            int p = p_nx;
+            const float bv = bv_nx, av = av_nx, dtb = dtb_nx, Ah = ah_nx;
             // the team's previous epilogue has finished reading the small area
             team_sync(team);
-            // ---- A: parents, gates, normalised q and k into B (hi / lo) ----------
-            int p = -1;
-            if (ttid < lc) p = a.parents[n0 + ttid];
-            float bv = 0.f, av = 0.f, dtb = 0.f, Ah = 0.f;
-            if (tw == 0 && lane < lc) {
-                const int64_t n = n0 + lane;
-                bv = __ldg(a.ba + n * a.ba_stride + h);
-                av = __ldg(a.ba + n * a.ba_stride + a.Hv + h);
-                dtb = __ldg(a.dt_bias + h);
-                Ah = __ldg(a.A + h);
-            }
-            // warp tw normalises B rows c = tw + 4 j: k^ of nodes tw + 4 j (j < 4)
-            // and q^ of the same nodes (j >= 4); lane l holds elements 4l..4l+3.
-            // The rows come from the stage the producer filled.
-            const bool staged = wait_or_abort(bars + B_SFULL + team, uint32_t(ut & 1), abort_flag);
-            float4 nvv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = tw + 4 * j, t = c & 15;
-                nvv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (staged && t < lc)
-                    nvv[j] = *reinterpret_cast<const float4 *>(sb + STAGE + ((c >> 4) * 4 + (lane >> 3)) * kStageBox +
-                                                               t * 128 + (lane & 7) * 16);
-            }
-            mbar_arrive(bars + B_SEMPTY);  // the stage may be refilled
+
+            // ---- A: parents and gates ---------------------------------------------
             if (ttid < lc) {
                 if (p < -1 || p >= ttid) {
                     gdn::record_status(a.status, GDN_DEV_BAD_PARENT);
-                    p = -1;  // outputs of a failed call are unspecified; keep the walk in bounds
+                    p = -1;  // outputs of a failed call are unspecified; keep the walks in bounds
                 }
                 par[ttid] = p;
             }
@@ -667,131 +823,130 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 dec_s[lane] = dec;
                 a.replay[(n * a.Hv + h) * a.rstride + 2 * D] = dec;
             }
+            // ---- B: Gram terms from tensor memory.  Warp tw holds G rows 16 tw ..
+            //      16 tw + 15 in lanes 0..15, row and column index a = [k | q | k_lo |
+            //      q_lo]: KA, QA take hi x hi + hi x lo (columns j and 32 + j), KB, QB
+            //      take lo x hi (column j); QQA, QQB the same for q_t . q_t. --------
+            const bool staged = wait_or_abort(bars + B_QFULL + team, uint32_t(ut & 1), abort_flag);
+            // warp-uniform: tcgen05.ld is warp-collective
+            const bool gready =
+                __all_sync(0xffffffffu, staged && wait_or_abort(bars + B_GFULL + team, uint32_t(ut & 1), abort_flag));
+            if (gready) {
+                gdn::tc_fence_after_sync();
+                const uint32_t grow = tmem + TEAM_COLS * team + GCOL + (uint32_t(tw * 32) << 16);
+                float d0[32], d1[32];
+                gdn::tmem_ld32(grow, d0);
+                gdn::tmem_ld32(grow + 32u, d1);
+                if (lane < kSeg) {
+                    const bool hi = tw < 2;
+                    float *dst = (tw == 0 ? ka : tw == 1 ? qa : tw == 2 ? kb : qb) + lane * kSeg;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = tw + 4 * j, t = c & 15;
-                float ss = nvv[j].x * nvv[j].x;
-                ss = fmaf(nvv[j].y, nvv[j].y, ss);
-                ss = fmaf(nvv[j].z, nvv[j].z, ss);
-                ss = fmaf(nvv[j].w, nvv[j].w, ss);
-                ss = gdn::warp_sum(ss);
-                nvv[j] = scale4(nvv[j], rsqrtf(ss + 1e-6f));
-                const float4 hi = make_float4(gdn::tf32_hi(nvv[j].x), gdn::tf32_hi(nvv[j].y),
-                                              gdn::tf32_hi(nvv[j].z), gdn::tf32_hi(nvv[j].w));
-                const float4 lo =
-                    make_float4(nvv[j].x - hi.x, nvv[j].y - hi.y, nvv[j].z - hi.z, nvv[j].w - hi.w);
-                const uint32_t off = sw_off(c, 4 * lane, kBChunk);
-                *reinterpret_cast<float4 *>(bhi_t + off) = hi;
-                *reinterpret_cast<float4 *>(blo_t + off) = lo;
-                if (c < kSeg && t < lc)
-                    *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride +
-                                                4 * lane) = nvv[j];
-            }
-            gdn::fence_proxy_async_smem();
-            mbar_arrive(bars + B_BREADY + team);
-
-            // ---- split the item's four S0 chunks as they land --------------------
-            for (int kb = 0; kb < 4; ++kb) {
-                if (!wait_or_abort(bars + B_FULL + 4 * team + kb, uint32_t(ut & 1), abort_flag)) continue;
-                float4 *raw = reinterpret_cast<float4 *>(sb + RAW + kb * kChunk);
-                float4 *lo = reinterpret_cast<float4 *>(sb + LO + kb * kChunk);
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int j = 4 * j4;
+                        *reinterpret_cast<float4 *>(dst + j) =
+                            hi ? make_float4(d0[j] + d1[j], d0[j + 1] + d1[j + 1], d0[j + 2] + d1[j + 2],
+                                             d0[j + 3] + d1[j + 3])
+                               : make_float4(d0[j], d0[j + 1], d0[j + 2], d0[j + 3]);
+                    }
+                    if (tw & 1) {
+                        float qq = 0.f;
 #pragma unroll
-                for (int j = 0; j < int(kChunk / 16 / 128); ++j) {
-                    const int f = ttid + 128 * j;
-                    const float4 x = raw[f];
-                    const float4 hi = make_float4(gdn::tf32_hi(x.x), gdn::tf32_hi(x.y), gdn::tf32_hi(x.z),
-                                                  gdn::tf32_hi(x.w));
-                    raw[f] = hi;
-                    lo[f] = make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
+                        for (int b = 0; b < kSeg; ++b)
+                            if (b == lane) qq = hi ? d0[kSeg + b] + d1[kSeg + b] : d0[kSeg + b];
+                        (hi ? qqa : qqb)[lane] = qq;
+                    }
                 }
-                gdn::fence_proxy_async_smem();
-                mbar_arrive(bars + B_SPLIT + 4 * team + kb);
             }
-            team_sync(team);  // parents and decays written by other warps of the team
+            team_sync(team);  // Gram terms, parents and decays of every node are in
 
-            // ---- C: path coefficients and Gamma; warp tw handles nodes tw + 4 m ---
-            // For node t and each ancestor j (walking up), with gamma = the decays
-            // strictly after j up to t:  cks[t][j] = gamma k^_j . k^_t,
-            // cqs[t][j] = gamma k^_j . q^_t;  cqs[t][t] = k^_t . q^_t;  Gamma_t = the
-            // product of all its decays.  Lane j < 16 owns entry j of each row.
+            // ---- C: path coefficients.  For node t and j on its path (j != t):
+            //      ck[t][j] = gamma k^_j . k^_t and cq[t][j] = gamma k^_j . q^_t with
+            //      gamma = the decays strictly after j up to t; cq[t][t] = k^_t . q^_t;
+            //      Gamma_t = all its decays, kept as Gamma_t / |k_t| and Gamma_t / |q_t|.
+            //      The eight lanes of node t = tw + 4 (lane >> 3) walk its path in
+            //      step; lane l owns entries j0 = 2 (l & 7) and j0 + 1 and writes
+            //      them over KA, QA (KA's diagonal, which other nodes read for |k_j|,
+            //      is written back unchanged). ---------------------------------------
+            float rk_t = 0.f;
             {
-                int cur[4];
-                float gam[4], ck[4], cq[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int t = tw + 4 * m;
-                    const bool valid = t < lc;
-                    const float self = gdn::warp_sum(gdn::fma4(nvv[m], nvv[4 + m], 0.f));
-                    cur[m] = valid ? par[t] : -1;
-                    gam[m] = valid ? dec_s[t] : 0.f;
-                    ck[m] = 0.f;
-                    cq[m] = (valid && lane == t) ? self : 0.f;
-                }
-                // the AND of the cursors is negative only once every one of them is -1
-                while ((cur[0] & cur[1] & cur[2] & cur[3]) >= 0) {
-                    float kk[4], kq[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        kk[m] = 0.f;
-                        kq[m] = 0.f;
-                        if (cur[m] >= 0) {
-                            const uint32_t oj = sw_off(cur[m], 4 * lane, kBChunk);
-                            const float4 kj = add4(*reinterpret_cast<const float4 *>(bhi_t + oj),
-                                                   *reinterpret_cast<const float4 *>(blo_t + oj));
-                            kk[m] = gdn::fma4(kj, nvv[m], 0.f);
-                            kq[m] = gdn::fma4(kj, nvv[4 + m], 0.f);
-                        }
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            kk[m] += __shfl_xor_sync(0xffffffffu, kk[m], o);
-                            kq[m] += __shfl_xor_sync(0xffffffffu, kq[m], o);
-                        }
-                    }
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        if (cur[m] >= 0) {
-                            if (lane == cur[m]) {
-                                ck[m] = gam[m] * kk[m];
-                                cq[m] = gam[m] * kq[m];
+                const int t = tw + 4 * (lane >> 3), j0 = 2 * (lane & 7);
+                float ck0 = 0.f, cq0 = 0.f, ck1 = 0.f, cq1 = 0.f;
+                if (t < lc) {
+                    const float rkt = rsqrtf(ka[t * (kSeg + 1)] + kb[t * (kSeg + 1)] + 1e-6f);
+                    const float rqt = rsqrtf(qqa[t] + qqb[t] + 1e-6f);
+                    if (j0 == t) ck0 = ka[t * (kSeg + 1)];
+                    if (j0 + 1 == t) ck1 = ka[t * (kSeg + 1)];
+                    float gam = 1.f;
+                    for (int cur = t;;) {
+                        gam *= dec_s[cur];
+                        cur = par[cur];
+                        if (cur < 0) break;
+                        if ((cur >> 1) == (j0 >> 1)) {
+                            const float rj = rsqrtf(ka[cur * (kSeg + 1)] + kb[cur * (kSeg + 1)] + 1e-6f);
+                            const float ck = gam * (ka[t * kSeg + cur] + kb[t * kSeg + cur]) * (rkt * rj);
+                            const float cq = gam * (qa[t * kSeg + cur] + qb[t * kSeg + cur]) * (rqt * rj);
+                            if (cur == j0) {
+                                ck0 = ck;
+                                cq0 = cq;
+                            } else {
+                                ck1 = ck;
+                                cq1 = cq;
                             }
-                            gam[m] *= dec_s[cur[m]];
-                            cur[m] = par[cur[m]];
                         }
                     }
+                    const float self = (qa[t * (kSeg + 1)] + qb[t * (kSeg + 1)]) * (rqt * rkt);
+                    if (j0 == t) cq0 = self;
+                    if (j0 + 1 == t) cq1 = self;
+                    if ((lane & 7) == 0) {
+                        gsk[t] = gam * rkt;
+                        gsq[t] = gam * rqt;
+                    }
+                    rk_t = rkt;
                 }
+                __syncwarp();  // every lane of the warp has read its Gram terms
+                if (t < lc) {
+                    *reinterpret_cast<float2 *>(ka + t * kSeg + j0) = make_float2(ck0, ck1);
+                    *reinterpret_cast<float2 *>(qa + t * kSeg + j0) = make_float2(cq0, cq1);
+                }
+            }
+            // replay: k^ of this warp's nodes, from B's raw rows
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int t = tw + 4 * m;
-                    if (t < lc) {
-                        if (lane < kSeg) {
-                            cks[t * kSeg + lane] = ck[m];
-                            cqs[t * kSeg + lane] = cq[m];
-                        }
-                        if (lane == 0) gam_s[t] = gam[m];
-                    }
-                }
+            for (int m = 0; m < 4; ++m) {
+                const int t = tw + 4 * m;
+                const float r = __shfl_sync(0xffffffffu, rk_t, 8 * m);
+                if (t < lc && staged)
+                    *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride + 4 * lane) =
+                        scale4(*reinterpret_cast<const float4 *>(bt_t + sw_off(t, 4 * lane, kBChunk)), r);
             }
             // v of this thread's row, loaded while the accumulators finish
             float vreg[kSeg];
 #pragma unroll
             for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? __ldg(a.xc + (n0 + t) * C + voff + row) : 0.0f;
-            team_sync(team);  // coefficients written by every warp of the team
+            team_sync(team);  // coefficients of every node are in
 
             // ---- E: per row, the nodes in order ------------------------------------
             // warp-uniform: tcgen05.ld is warp-collective
             const bool ready =
                 __all_sync(0xffffffffu, wait_or_abort(bars + B_ACCFULL + team, uint32_t(ut & 1), abort_flag));
             if (ready) {
+                // the products are done and the team has finished reading B: its
+                // next q/k rows may land there while this epilogue runs
+                gdn::fence_proxy_async_smem();
+                issue_qk(v + 2);
+            }
+            prefetch(v + 2);
+            if (ready) {
                 gdn::tc_fence_after_sync();
-                const uint32_t trow = tmem + TEAM_COLS * team + (uint32_t((warp & 3) * 32) << 16);
-                // D = sum over the 8 partial accumulators, added in fp32
+                const uint32_t trow = tmem + TEAM_COLS * team + (uint32_t(tw * 32) << 16);
+                // D = the sum of the partial accumulators, added in fp32: the
+                // 2^10 A_lo B_hi part first (scaled back, exactly), then A_hi B_hi
+                // and A_hi B_lo of both K-halves
                 float dv[32], p1[32];
-                gdn::tmem_ld32(trow + 0, dv);
+                gdn::tmem_ld32(trow + LHCOL, dv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dv[i] *= 1.0f / kLoScale;
 #pragma unroll 1
-                for (int part = 1; part < 8; ++part) {
+                for (int part = 0; part < 4; ++part) {
                     gdn::tmem_ld32(trow + 32u * part, p1);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) dv[i] += p1[i];
@@ -799,49 +954,51 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 gdn::tc_fence_before_sync();
                 mbar_arrive(bars + B_ACCEMPTY + team);  // the accumulators may be overwritten
 
-                float u[kSeg];
+                // S' k_t and o_t / q_scale each accumulate as a packed pair over
+                // even and odd j (ck, cq pairs times (u_2p, u_2p+1)), folded at
+                // the end.  up[p] holds (u_2p, u_2p+1), with zeros not yet known.
+                uint64_t up[kSeg / 2];
+                float uprev = 0.f;
 #pragma unroll
                 for (int t = 0; t < kSeg; ++t) {
-                    u[t] = 0.f;
+                    if (!(t & 1)) up[t / 2] = 0;
                     if (t < lc) {
                         const int64_t n = n0 + t;
-                        float sk = gam_s[t] * dv[t];
-                        float oq = gam_s[t] * dv[kSeg + t];
+                        uint64_t sk2 = gdn::f2pack(gsk[t] * dv[t], 0.f), oq2 = gdn::f2pack(gsq[t] * dv[kSeg + t], 0.f);
 #pragma unroll
-                        for (int j4 = 0; j4 < (t + 4) / 4; ++j4) {
-                            const float4 ckv = *reinterpret_cast<const float4 *>(cks + t * kSeg + 4 * j4);
-                            const float4 cqv = *reinterpret_cast<const float4 *>(cqs + t * kSeg + 4 * j4);
-                            if (4 * j4 + 0 < t) sk = fmaf(ckv.x, u[4 * j4 + 0], sk);
-                            if (4 * j4 + 1 < t) sk = fmaf(ckv.y, u[4 * j4 + 1], sk);
-                            if (4 * j4 + 2 < t) sk = fmaf(ckv.z, u[4 * j4 + 2], sk);
-                            if (4 * j4 + 3 < t) sk = fmaf(ckv.w, u[4 * j4 + 3], sk);
-                            if (4 * j4 + 0 < t) oq = fmaf(cqv.x, u[4 * j4 + 0], oq);
-                            if (4 * j4 + 1 < t) oq = fmaf(cqv.y, u[4 * j4 + 1], oq);
-                            if (4 * j4 + 2 < t) oq = fmaf(cqv.z, u[4 * j4 + 2], oq);
-                            if (4 * j4 + 3 < t) oq = fmaf(cqv.w, u[4 * j4 + 3], oq);
+                        for (int j4 = 0; j4 < (t + 3) / 4; ++j4) {
+                            // pairs 2 j4 and 2 j4 + 1; a pair holding j = t sees u_t = 0
+                            const ulonglong2 ck = *reinterpret_cast<const ulonglong2 *>(ka + t * kSeg + 4 * j4);
+                            const ulonglong2 cq = *reinterpret_cast<const ulonglong2 *>(qa + t * kSeg + 4 * j4);
+                            sk2 = gdn::fma2(ck.x, up[2 * j4], sk2);
+                            oq2 = gdn::fma2(cq.x, up[2 * j4], oq2);
+                            if (4 * j4 + 2 < t) {
+                                sk2 = gdn::fma2(ck.y, up[2 * j4 + 1], sk2);
+                                oq2 = gdn::fma2(cq.y, up[2 * j4 + 1], oq2);
+                            }
                         }
-                        u[t] = beta_s[t] * (vreg[t] - sk);
-                        oq = fmaf(cqs[t * kSeg + t], u[t], oq);
-                        a.o[(n * a.Hv + h) * D + row] = a.q_scale * oq;
-                        a.replay[(n * a.Hv + h) * a.rstride + D + row] = u[t];
+                        const float2 sk = gdn::f2unpack(sk2), oq = gdn::f2unpack(oq2);
+                        const float ut = beta_s[t] * (vreg[t] - (sk.x + sk.y));
+                        up[t / 2] = (t & 1) ? gdn::f2pack(uprev, ut) : gdn::f2pack(ut, 0.f);
+                        uprev = ut;
+                        const float o = fmaf(qa[t * kSeg + t], ut, oq.x + oq.y);
+                        a.o[(n * a.Hv + h) * D + row] = a.q_scale * o;
+                        a.replay[(n * a.Hv + h) * a.rstride + D + row] = ut;
                     }
                 }
             }
             // after a timeout the team keeps looping (every wait now returns at
             // once) so that all four warps meet at each team barrier
         }
+        // after a timeout, a q/k copy may still be in flight: wait for it (bounded)
+        if (*abort_flag && qk_issued > 0)
+            gdn::mbar_wait_bounded(bars + B_QFULL + team, uint32_t((qk_issued - 1) & 1));
     }
 
     // ---- tear-down -------------------------------------------------------------
-    if (*abort_flag) {
-        if (tid == 0) {
-            gdn::record_status(a.status, GDN_DEV_TIMEOUT);
-            // drain whatever may still be in flight (bounded) before release
-            for (int kb = 0; kb < 4; ++kb) gdn::mbar_wait_bounded(bars + B_EMPTY + kb, uint32_t((nv - 1) & 1));
-        }
-    }
     gdn::tc_fence_before_sync();
     __syncthreads();
+    if (tid == 0 && *abort_flag) gdn::record_status(a.status, GDN_DEV_TIMEOUT);
     if (warp == 1) {
         gdn::tc_fence_after_sync();
         gdn::tmem_dealloc(tmem, TMEM_COLS);
@@ -896,7 +1053,8 @@ int sm_count() {
 }
 
 // xc viewed as [N rows][C floats]; boxes of [16 rows][32 floats] (the q or k
-// rows of one sequence's 16 nodes, 32 columns at a time)
+// rows of one sequence's 16 nodes, one K-chunk) in the 128-byte swizzle, so a
+// box lands as 16 rows of the tensor cores' K-major operand
 int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C) {
     auto enc = tensor_map_encoder();
     if (!enc) return GDN_ERR_TMA;
@@ -905,7 +1063,7 @@ int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C) {
     cuuint32_t box[2] = {32, 16};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(xc), gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
 }
