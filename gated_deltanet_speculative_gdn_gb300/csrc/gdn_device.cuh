@@ -178,6 +178,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float x, float y) {
     return r;
 }
 
+// The two fp16 of a packed pair as floats (low half first).
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+    float2 r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(v));
+    return r;
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {

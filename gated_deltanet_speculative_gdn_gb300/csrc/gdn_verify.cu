@@ -449,20 +449,20 @@ constexpr int kThreadsWS = kWarps * 32;
 constexpr int kSplit0 = 2, kSplitThreads = 64;     // splitter warps 2-3
 constexpr int kTeam0 = 4;                          // team t: warps 4 + 4t .. 7 + 4t
 constexpr int kMaxItems = 64;                      // items per CTA
-constexpr int NR = 6;                              // S0 ring depth (K-chunks)
+constexpr int NR = 5;                              // S0 ring depth (K-chunks)
 constexpr int NLP = 2;                             // lo ring depth (two-chunk fp16 tiles)
 constexpr uint32_t kChunk = 128 * 128;             // one S0 K-chunk: 128 rows x 32 fp32
 constexpr uint32_t kLoTile = 128 * 128;            // S0 lo of two K-chunks: 128 rows x 64 fp16
 constexpr uint32_t kBChunk = 64 * 128;             // one B K-chunk: rows 0-31 hi, 32-63 lo (fp32)
 constexpr uint32_t kBTeam = 4 * kBChunk;           // one team's tf32 B
-constexpr uint32_t kBHTile = 32 * 128;             // fp16 B of two K-chunks: 32 rows x 64 fp16
-constexpr uint32_t kBHTeam = 2 * kBHTile;          // one team's fp16 B
+constexpr uint32_t kGATile = 64 * 128;             // fp16 B of two K-chunks: 64 rows x 64 fp16
+constexpr uint32_t kGATeam = 2 * kGATile;          // one team's fp16 B: rows [k | q | k_lo | q_lo]
 constexpr uint32_t kQKBox = 16 * 128;              // 16 rows of k or q, one K-chunk
 constexpr uint32_t RAW = 0;
 constexpr uint32_t LO = RAW + NR * kChunk;
 constexpr uint32_t BT = LO + NLP * kLoTile;        // per team: q/k rows normalised in place, lo below
-constexpr uint32_t BH = BT + 2 * kBTeam;           // per team
-constexpr uint32_t SMALL = BH + 2 * kBHTeam;
+constexpr uint32_t GA = BT + 2 * kBTeam;           // per team
+constexpr uint32_t SMALL = GA + 2 * kGATeam;
 // per-team small area (4-byte words): the Gram terms as partial sums from the
 // four tensor-memory lane quarters, KA + KB = k_t . k_j and QA + QB = q_t . k_j
 // ([16][16]; the path coefficients ck, cq then overwrite KA, QA in place),
@@ -494,13 +494,17 @@ static_assert((W_BARS % 2) == 0, "mbarriers are 8-byte aligned");
 // tf32 x tf32 with N = 64 and fp16 x fp16 with N = 32
 constexpr uint32_t IDESC_TF32 = (1u << 4) | (2u << 7) | (2u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t IDESC_F16 = (1u << 4) | (0u << 7) | (0u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-// the Gram terms: tf32, M = 64, N = 64, both operands the team's stacked B
-constexpr uint32_t IDESC_GRAM = (1u << 4) | (2u << 7) | (2u << 10) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
+// the Gram terms: fp16, M = 64, N = 64, both operands the team's fp16 B
+constexpr uint32_t IDESC_GRAM = (1u << 4) | (0u << 7) | (0u << 10) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
 constexpr float kLoScale = 1024.0f;                // A_lo is stored as fp16(2^10 A_lo)
+// the fp16 B holds hi = fp16(2^-8 x) (range up to ~1.7e7) and lo =
+// fp16(2^11 (2^-8 x - hi)), so x = 2^8 (hi + 2^-11 lo) to ~2^-22
+constexpr float kBScale = 1.0f / 256.0f, kBLoScale = 2048.0f;
 // Team t's accumulators start at column 256 t: K-half kh (chunks 2 kh, 2 kh + 1)
 // owns columns 64 kh .. 64 kh + 63, A_hi B_hi in the first 32 and A_hi B_lo in
-// the last 32; 2^10 A_lo B_hi of all four K-chunks sits at 128.  The Gram terms
-// G = B B^T (M = 64: row a of G in lane 32 (a / 16) + a % 16) sit at 192.
+// the last 32; 2^10 A_lo 2^-8 B_hi of all four K-chunks sits at 128.  The
+// Gram terms G of the fp16 B with itself (M = 64: row a of G in lane
+// 32 (a / 16) + a % 16) sit at 192.
 constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256, LHCOL = 128, GCOL = 192;
 
 __device__ __forceinline__ uint32_t sw_off(int row, int k, uint32_t chunk) {
@@ -634,14 +638,14 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 if (!wait_or_abort(bars + B_BREADY + t, uint32_t(ut & 1), abort_flag)) break;
                 if (ut > 0 && !wait_or_abort(bars + B_ACCEMPTY + t, uint32_t((ut - 1) & 1), abort_flag)) break;
                 const uint32_t dacc = tmem + TEAM_COLS * t;
-                const uint32_t bt0 = sbase + BT + t * kBTeam, bh0 = sbase + BH + t * kBHTeam;
-                // Gram terms of B's 64 rows [k | q | k_lo | q_lo] with themselves:
-                // hi x hi, hi x lo and lo x hi all appear in the one product
-                for (int kb = 0; kb < 4; ++kb) {
-                    uint64_t gd = gdn::desc_sw128(bt0 + kb * kBChunk);
+                const uint32_t bt0 = sbase + BT + t * kBTeam, ga0 = sbase + GA + t * kGATeam;
+                // Gram terms of the fp16 B's 64 rows [k | q | k_lo | q_lo] with
+                // themselves: hi x hi, hi x lo and lo x hi all appear in the one product
+                for (int kt = 0; kt < 2; ++kt) {
+                    uint64_t gd = gdn::desc_sw128(ga0 + kt * kGATile);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks, gd += 2)
-                        gdn::mma_tf32(dacc + GCOL, gd, gd, IDESC_GRAM, (kb | ks) != 0);
+                        gdn::mma_f16(dacc + GCOL, gd, gd, IDESC_GRAM, (kt | ks) != 0);
                 }
                 gdn::mma_commit(bars + B_GFULL + t);
                 for (int kb = 0; kb < 4; ++kb) {
@@ -666,7 +670,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                     gdn::tc_fence_after_sync();
                     // this chunk's 32 K-columns are the (kb & 1) half of the two-chunk tiles
                     uint64_t alo = gdn::desc_sw128(sbase + LO + l * kLoTile + 64u * (kb & 1));
-                    uint64_t bh = gdn::desc_sw128(bh0 + (kb >> 1) * kBHTile + 64u * (kb & 1));
+                    uint64_t bh = gdn::desc_sw128(ga0 + (kb >> 1) * kGATile + 64u * (kb & 1));  // rows 0-31
 #pragma unroll 1
                     for (int ks = 0; ks < 2; ++ks, alo += 2, bh += 2)
                         gdn::mma_f16(dacc + LHCOL, alo, bh, IDESC_F16, (kb | ks) != 0);
@@ -699,18 +703,26 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         bool ok = true;
         for (int v = 0; v < nv && ok; ++v) {
             const int t = v & 1;
-            // B: rows c (k of node c, then q of node c - 16) of each K-chunk; lo
-            // below them (rows 32 + c, same swizzle phase), fp16 copy beside
+            // B: rows c (k of node c, then q of node c - 16) of each K-chunk; tf32
+            // lo below them (rows 32 + c, same swizzle phase); the fp16 B beside
             if (!wait_or_abort(bars + B_QFULL + t, uint32_t((v >> 1) & 1), abort_flag)) break;
             {
-                unsigned char *bt = sb + BT + t * kBTeam, *bh = sb + BH + t * kBHTeam;
+                unsigned char *bt = sb + BT + t * kBTeam, *ga = sb + GA + t * kGATeam;
 #pragma unroll 4
                 for (int j = 0; j < 16; ++j) {
                     const int kb = j >> 2, c = (st >> 3) + 8 * (j & 3), uu = st & 7;
                     unsigned char *p = bt + kb * kBChunk + c * 128 + uu * 16;
                     const float4 x = *reinterpret_cast<const float4 *>(p);
                     *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
-                    *reinterpret_cast<uint2 *>(bh + sw_off_h(c, 32 * kb + 4 * (uu ^ (c & 7)), kBHTile)) = f16x4(x);
+                    // fp16 hi of 2^-8 x, and 2^11 times what it misses (exact before rounding)
+                    const int kk = 32 * kb + 4 * (uu ^ (c & 7));
+                    const float4 y = scale4(x, kBScale);
+                    const uint2 hh = f16x4(y);
+                    const float2 h01 = gdn::unpack_f16x2(hh.x), h23 = gdn::unpack_f16x2(hh.y);
+                    const float4 r = make_float4((y.x - h01.x) * kBLoScale, (y.y - h01.y) * kBLoScale,
+                                                 (y.z - h23.x) * kBLoScale, (y.w - h23.y) * kBLoScale);
+                    *reinterpret_cast<uint2 *>(ga + sw_off_h(c, kk, kGATile)) = hh;
+                    *reinterpret_cast<uint2 *>(ga + sw_off_h(32 + c, kk, kGATile)) = f16x4(r);
                 }
                 gdn::fence_proxy_async_smem();
                 mbar_arrive(bars + B_BREADY + t);
@@ -825,8 +837,10 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             }
             // ---- B: Gram terms from tensor memory.  Warp tw holds G rows 16 tw ..
             //      16 tw + 15 in lanes 0..15, row and column index a = [k | q | k_lo |
-            //      q_lo]: KA, QA take hi x hi + hi x lo (columns j and 32 + j), KB, QB
-            //      take lo x hi (column j); QQA, QQB the same for q_t . q_t. --------
+            //      q_lo] of the fp16 B: KA, QA take hi x hi + 2^-11 hi x lo (columns
+            //      j and 32 + j), KB, QB take 2^-11 lo x hi (column j), all times
+            //      2^16 (the 2^-8 scale of both sides); QQA, QQB the same for
+            //      q_t . q_t. ----------------------------------------------------------
             const bool staged = wait_or_abort(bars + B_QFULL + team, uint32_t(ut & 1), abort_flag);
             // warp-uniform: tcgen05.ld is warp-collective
             const bool gready =
@@ -839,20 +853,22 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 gdn::tmem_ld32(grow + 32u, d1);
                 if (lane < kSeg) {
                     const bool hi = tw < 2;
+                    // 2^16 undoes the 2^-8 scale on both sides; 2^-11 the lo scale
+                    constexpr float kG = 1.0f / (kBScale * kBScale), kX = 1.0f / kBLoScale, kGX = kG * kX;
                     float *dst = (tw == 0 ? ka : tw == 1 ? qa : tw == 2 ? kb : qb) + lane * kSeg;
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
                         const int j = 4 * j4;
                         *reinterpret_cast<float4 *>(dst + j) =
-                            hi ? make_float4(d0[j] + d1[j], d0[j + 1] + d1[j + 1], d0[j + 2] + d1[j + 2],
-                                             d0[j + 3] + d1[j + 3])
-                               : make_float4(d0[j], d0[j + 1], d0[j + 2], d0[j + 3]);
+                            hi ? make_float4(kG * fmaf(d1[j], kX, d0[j]), kG * fmaf(d1[j + 1], kX, d0[j + 1]),
+                                             kG * fmaf(d1[j + 2], kX, d0[j + 2]), kG * fmaf(d1[j + 3], kX, d0[j + 3]))
+                               : make_float4(kGX * d0[j], kGX * d0[j + 1], kGX * d0[j + 2], kGX * d0[j + 3]);
                     }
                     if (tw & 1) {
                         float qq = 0.f;
 #pragma unroll
                         for (int b = 0; b < kSeg; ++b)
-                            if (b == lane) qq = hi ? d0[kSeg + b] + d1[kSeg + b] : d0[kSeg + b];
+                            if (b == lane) qq = hi ? kG * fmaf(d1[kSeg + b], kX, d0[kSeg + b]) : kGX * d0[kSeg + b];
                         (hi ? qqa : qqb)[lane] = qq;
                     }
                 }
@@ -939,12 +955,12 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 gdn::tc_fence_after_sync();
                 const uint32_t trow = tmem + TEAM_COLS * team + (uint32_t(tw * 32) << 16);
                 // D = the sum of the partial accumulators, added in fp32: the
-                // 2^10 A_lo B_hi part first (scaled back, exactly), then A_hi B_hi
-                // and A_hi B_lo of both K-halves
+                // 2^10 A_lo 2^-8 B_hi part first (scaled back, exactly), then
+                // A_hi B_hi and A_hi B_lo of both K-halves
                 float dv[32], p1[32];
                 gdn::tmem_ld32(trow + LHCOL, dv);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) dv[i] *= 1.0f / kLoScale;
+                for (int i = 0; i < 32; ++i) dv[i] *= 1.0f / (kLoScale * kBScale);
 #pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     gdn::tmem_ld32(trow + 32u * part, p1);
