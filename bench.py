@@ -10,9 +10,14 @@ pools persist across steps, as in a real decode loop.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is nodes/s over all ranks (each rank a
-replica with its own pools: weak scaling).  L2 is flushed (256 MB write)
-before every timed step; each step is timed with CUDA events on the launching
-stream, per kernel as well.  `e2e` repeats the measurement through the same C
+replica with its own pools: weak scaling).  L2 is flushed before every timed
+step: a 256 MB write, then a 256 MB read of another buffer, so the flush's
+dirty lines are written back before the step starts (--l2-dirty skips the
+read and leaves them to the step).  Each step is timed with CUDA events on the
+launching stream around the whole step (`value`, `ms_per_step`), and in a
+second pass of the same K steps with events between the kernels as well (the
+per-kernel split and roofline; those events stop the kernels' launches from
+overlapping each other's tails).  `e2e` repeats the measurement through the same C
 ABI from pinned host buffers, with the step's inputs copied in and its output
 copied out inside the timed region.  `cpu_baseline` times the oracle on the
 host cores on a bounded sample of the same workload.  `--impl reference` times
@@ -41,6 +46,31 @@ METRIC = "GDN tree-verify+commit nodes/s and achieved HBM GB/s (% of GB300 peak)
 HEADLINE = "grouped_tree16"
 N_ROUNDS = 100
 L2_FLUSH_BYTES = 256 << 20
+L2_DIRTY = False  # --l2-dirty: flush by the write alone
+
+
+class L2Flush:
+    """Evicts the step's data from L2 between timed steps: a write of a buffer
+    larger than L2, then (unless L2_DIRTY) a read of a second one, so that the
+    write's dirty lines drain to DRAM outside the timed region."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = None if L2_DIRTY else torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.zeros((), dtype=torch.float32, device=device)
+
+    def __call__(self, i):
+        self.w.fill_(float(i))
+        if self.r is not None:
+            self.sink.add_(self.r.sum())
+
+    @staticmethod
+    def describe_static():
+        if L2_DIRTY:
+            return "flushed before every timed step (256 MB write; its dirty lines drain during the step)"
+        return ("flushed before every timed step (256 MB write, then a 256 MB read of another buffer so "
+                "the write's dirty lines drain before the step)")
 
 
 def measured_peaks():
@@ -226,10 +256,10 @@ def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int
     import torch
     sp = W.sweep_spec(variant, rounds=N_ROUNDS)
     wl = DeviceWorkload(sp, min(N_ROUNDS, max(steps + warmup, 1)), device, seed_offset)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
     nr = len(wl.rounds)
     for i in range(warmup):
-        flush.fill_(float(i))
+        flush(i)
         wl.step(i % nr)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
@@ -240,24 +270,38 @@ def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int
         time.sleep(0.3)
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.fill_(float(i))                        # L2 flush, outside the step's events
+        flush(i)                                     # L2 flush, outside the step's events
         wl.step((warmup + i) % nr, ev[i])
         ends[i].record()
+    torch.cuda.synchronize()
+    # The same K steps again with events only around each whole step: events
+    # between the kernels would stop a kernel's launch from overlapping the
+    # previous one's tail (programmatic dependent launch), so the step time
+    # comes from this pass and the per-kernel split from the one above.
+    whole = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush(i)
+        whole[i][0].record()
+        wl.step((warmup + i) % nr)
+        whole[i][1].record()
     torch.cuda.synchronize()
     if sampler:
         sampler.__exit__()
     assert int(wl.status.item()) == 0, wl.G.gdn_status_str(int(wl.status.item()))
     per = {"conv": [], "verify": [], "commit": []}
-    step_ms = []
+    step_ms = [a.elapsed_time(b) for a, b in whole]
+    step_ms_kernel_events = []
     for i in range(steps):
         e = ev[i] + [ends[i]]
         per["conv"].append(e[0].elapsed_time(e[1]))
         per["verify"].append(e[1].elapsed_time(e[2]))
         per["commit"].append(e[2].elapsed_time(e[3]))
-        step_ms.append(e[0].elapsed_time(e[3]))
+        step_ms_kernel_events.append(e[0].elapsed_time(e[3]))
     bytes_ = [algo_bytes(sp, wl.host_rounds[(warmup + i) % nr].parents, wl.host_rounds[(warmup + i) % nr].node_off,
                          wl.host_rounds[(warmup + i) % nr].accepted) for i in range(steps)]
-    out = {"sp": sp, "wl": wl, "step_ms": step_ms, "per": per, "bytes": bytes_,
+    out = {"sp": sp, "wl": wl, "step_ms": step_ms, "step_ms_kernel_events": step_ms_kernel_events, "per": per,
+           "bytes": bytes_,
            "clocks": sampler.summary() if sampler else None}
     if e2e:
         out["e2e"] = time_e2e(wl, steps, warmup)
@@ -277,7 +321,7 @@ def time_e2e(wl: DeviceWorkload, steps: int, warmup: int, host_rounds: int = 8):
     st_host = torch.empty(1, dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
     d2h = wl.o.numel() * wl.o.element_size() + 4
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=wl.device)
+    flush = L2Flush(wl.device)
 
     def one(r):
         for k, v in host[r].items():
@@ -291,7 +335,7 @@ def time_e2e(wl: DeviceWorkload, steps: int, warmup: int, host_rounds: int = 8):
     torch.cuda.synchronize()
     times = []
     for i in range(steps):
-        flush.fill_(float(i))
+        flush(i)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         one((warmup + i) % nr)
@@ -347,7 +391,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variants", default="all", help="'all' or a comma list of sweep variants")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-dirty", action="store_true", help="flush L2 by the write alone (no draining read)")
     args = ap.parse_args()
+    global L2_DIRTY
+    L2_DIRTY = bool(args.l2_dirty)
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
     rank = int(os.environ.get("RANK", "0"))
@@ -433,11 +480,12 @@ def main():
                                f"H_v=32, d=128, d_conv=4, one layer, {N_ROUNDS} rounds",
                    "n_seqs": 64, "nodes_per_step": N, "h_k": 16, "h_v": 32, "d": 128,
                    "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step (256 MB write)"},
+                   "l2": L2Flush.describe_static()},
         "hbm": {"step_algo_bytes": int(step_bytes),
                 "step_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
-                "peak_gbs": peak, "peak_kind": peak_kind},
+                "peak_gbs": peak, "peak_kind": peak_kind,
+                "ms_per_step_with_kernel_events": round(statistics.mean(head["step_ms_kernel_events"]), 5)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind},

@@ -20,8 +20,9 @@
 //                 S = Gamma S0 + sum_j c_j u_j k_j^T,   c_j = prod of decays after j
 //             which equals applying S <- decay_j S + u_j k_j^T root first.  The
 //             state rows are held in registers (coalesced 128-bit loads and
-//             stores); each warp also copies its share of the accepted node's
-//             window into the slot's conv history.
+//             stores), the path's replay rows are staged in shared memory, and
+//             the CTA also copies its share of the accepted node's window into
+//             the slot's conv history.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
@@ -43,6 +44,8 @@ struct CommitArgs {
 };
 
 __global__ void __launch_bounds__(256) commit_preflight_kernel(const CommitArgs a) {
+    gdn::grid_dep_launch();
+    gdn::grid_dep_wait();  // status
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= a.S) return;
@@ -75,130 +78,161 @@ __global__ void __launch_bounds__(256) commit_preflight_kernel(const CommitArgs 
     if (err && lane == 0) gdn::record_status(a.status, err);
 }
 
-// Apply: every warp works alone, with no block barrier.  A CTA of four warps
-// covers 32 state rows of one (head, sequence); warp w owns 8 of them (lane l:
-// row group l / (d/4), float4 column group l % (d/4)).  The warp reads the
-// sequence header, issues the loads of its rows at once, walks the accepted
-// path with register shuffles (parents two per lane), forms the closed-form
-// coefficients with a warp scan of the path's decays, and applies the path's
-// rank-one terms from the replay rows (shared by the CTAs of the head: L1/L2
-// hits), the next step's rows loading while the current one is applied.
+// Apply: a CTA of four warps covers 32 state rows of one (head, sequence);
+// warp w owns 8 of them (lane l: row group l / (d/4), float4 column group
+// l % (d/4)) and loads them into registers first.  Meanwhile warp 0 walks the
+// accepted path (parents two per lane, walked by shuffles), forms the
+// closed-form coefficients with a warp scan of the path's decays and leaves
+// them in shared memory, and the other warps copy their share of the accepted
+// node's window.  The path's replay rows (k^_j and this CTA's slice of u_j)
+// are then staged into shared memory together, kBatch entries at a time, so
+// the CTA waits for one round trip per batch rather than one per entry, and
+// every warp applies them root first from there.
 constexpr int kWarpRows = 8;                      // state rows per warp
 constexpr int kApplyWarps = 4;
 constexpr int kCtaRows = kWarpRows * kApplyWarps; // state rows per CTA
+constexpr int kBatch = 16;                        // path entries staged at a time
 
 template <int D>
-__global__ void __launch_bounds__(kApplyWarps * 32) commit_apply_warp_kernel(const CommitArgs a) {
+__global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const CommitArgs a) {
     constexpr int DV4 = D / 4;               // float4 chunks per row (<= 32)
     constexpr int RI = 32 / DV4;             // rows one warp instruction covers
     constexpr int NF = kWarpRows / RI;       // float4 per lane
     constexpr int CPH = (D + kCtaRows - 1) / kCtaRows;  // CTAs per head
+    constexpr int CR = D < kCtaRows ? D : kCtaRows;     // state rows of a CTA
     static_assert(NF >= 1, "d >= 16");
+    __shared__ float4 kst[kBatch][DV4];      // k^_j rows of the batch
+    __shared__ float ust[kBatch][CR];        // u_j of the CTA's rows
+    __shared__ int nodes[gdn::kMaxSeqNodes]; // path, leaf first
+    __shared__ float coef[gdn::kMaxSeqNodes];
+    __shared__ float gam_s;
+    __shared__ int m_s;
+
     const int hq = blockIdx.x, s = blockIdx.y;
     const int h = hq / CPH, q = hq % CPH;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned full = 0xffffffffu;
-    const int rbase = q * kCtaRows + warp * kWarpRows;  // first row of the warp
+    const int rcta = q * kCtaRows, rbase = rcta + warp * kWarpRows;  // first row of the CTA, the warp
+    const bool has_rows = rbase < D;  // d = 16: two warps hold no rows
 
     // the preflight (earlier on this stream) has checked every index; the range
     // tests here only keep the loads below in bounds
-    const int st = *reinterpret_cast<volatile int32_t *>(a.status);
+    gdn::grid_dep_launch();
     const int acc = a.accepted[s], n0 = a.node_off[s], n1 = a.node_off[s + 1], slot = a.slot_map[s];
+    gdn::grid_dep_wait();  // status, the state pool and the replay rows
+    const int st = *reinterpret_cast<volatile int32_t *>(a.status);
     if (!(st == 0 && acc >= 0 && n0 >= 0 && n1 <= a.N && acc < n1 - n0 && acc < gdn::kMaxSeqNodes && slot >= 0 &&
           slot < a.P))
-        return;
-
-    {
-        // this warp's share of the window copy: conv_hist[slot] <- win[accepted]
-        const int64_t total4 = int64_t(3) * a.C / 4;
-        const int64_t parts = int64_t(a.Hv) * CPH * kApplyWarps;
-        const int64_t per = (total4 + parts - 1) / parts;
-        const int64_t lo = ((int64_t(h) * CPH + q) * kApplyWarps + warp) * per, hi = min(total4, lo + per);
-        const float4 *wsrc = reinterpret_cast<const float4 *>(a.win + (int64_t(n0) + acc) * 3 * a.C);
-        float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(slot) * 3 * a.C);
-        for (int64_t i = lo + lane; i < hi; i += 32) hdst[i] = __ldg(wsrc + i);
-    }
-    if (rbase >= D) return;  // d = 16: two warps hold no rows
+        return;  // the whole CTA: the condition does not depend on the thread
 
     const int kc = lane % DV4, ro = lane / DV4;
     float *sbase = a.ssm + (int64_t(slot) * a.Hv + h) * D * D;
     float4 sv[NF];
+    if (has_rows) {
 #pragma unroll
-    for (int f = 0; f < NF; ++f)
-        sv[f] = *reinterpret_cast<const float4 *>(sbase + (rbase + ro + RI * f) * D + 4 * kc);
-
-    // path, leaf first: lane i holds entry i (register lo) and i + 32 (hi)
-    const int p_lo = lane <= acc ? a.parents[n0 + lane] : -1;
-    const int p_hi = lane + 32 <= acc ? a.parents[n0 + lane + 32] : -1;
-    int node_lo = -1, node_hi = -1, m = 0;
-    for (int cur = acc; cur >= 0; ++m) {
-        if (lane == (m & 31)) {
-            if (m < 32) node_lo = cur; else node_hi = cur;
-        }
-        cur = __shfl_sync(full, cur < 32 ? p_lo : p_hi, cur & 31);
+        for (int f = 0; f < NF; ++f)
+            sv[f] = *reinterpret_cast<const float4 *>(sbase + (rbase + ro + RI * f) * D + 4 * kc);
     }
-    // coefficient of leaf-first entry i = product of the decays of entries 0..i-1
-    const float *dbase = a.replay + int64_t(h) * a.rstride + 2 * D;
     const int64_t rnode = int64_t(a.Hv) * a.rstride;
-    const float d_lo = node_lo >= 0 ? __ldg(dbase + (int64_t(n0) + node_lo) * rnode) : 1.0f;
-    const float d_hi = node_hi >= 0 ? __ldg(dbase + (int64_t(n0) + node_hi) * rnode) : 1.0f;
-    float x_lo = d_lo, x_hi = d_hi;  // inclusive scans
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y_lo = __shfl_up_sync(full, x_lo, o), y_hi = __shfl_up_sync(full, x_hi, o);
-        if (lane >= o) {
-            x_lo *= y_lo;
-            x_hi *= y_hi;
-        }
-    }
-    const float tot_lo = __shfl_sync(full, x_lo, 31);
-    float c_lo = __shfl_up_sync(full, x_lo, 1), c_hi = __shfl_up_sync(full, x_hi, 1);
-    if (lane == 0) {
-        c_lo = 1.0f;
-        c_hi = 1.0f;
-    }
-    c_hi *= tot_lo;
-    const float gam = tot_lo * __shfl_sync(full, x_hi, 31);  // all m decays
+    const float *rbase_h = a.replay + (int64_t(n0) * a.Hv + h) * a.rstride;  // node 0 of the sequence, head h
 
+    if (warp == 0) {
+        // path, leaf first: lane i holds entry i (register lo) and i + 32 (hi)
+        const int p_lo = lane <= acc ? a.parents[n0 + lane] : -1;
+        const int p_hi = lane + 32 <= acc ? a.parents[n0 + lane + 32] : -1;
+        int node_lo = -1, node_hi = -1, m = 0;
+        for (int cur = acc; cur >= 0; ++m) {
+            if (lane == (m & 31)) {
+                if (m < 32) node_lo = cur; else node_hi = cur;
+            }
+            cur = __shfl_sync(full, cur < 32 ? p_lo : p_hi, cur & 31);
+        }
+        // coefficient of leaf-first entry i = product of the decays of entries 0..i-1
+        const float d_lo = node_lo >= 0 ? __ldg(rbase_h + node_lo * rnode + 2 * D) : 1.0f;
+        const float d_hi = node_hi >= 0 ? __ldg(rbase_h + node_hi * rnode + 2 * D) : 1.0f;
+        float x_lo = d_lo, x_hi = d_hi;  // inclusive scans
 #pragma unroll
-    for (int f = 0; f < NF; ++f) {
-        sv[f].x *= gam; sv[f].y *= gam; sv[f].z *= gam; sv[f].w *= gam;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y_lo = __shfl_up_sync(full, x_lo, o), y_hi = __shfl_up_sync(full, x_hi, o);
+            if (lane >= o) {
+                x_lo *= y_lo;
+                x_hi *= y_hi;
+            }
+        }
+        const float tot_lo = __shfl_sync(full, x_lo, 31);
+        float c_lo = __shfl_up_sync(full, x_lo, 1), c_hi = __shfl_up_sync(full, x_hi, 1);
+        if (lane == 0) {
+            c_lo = 1.0f;
+            c_hi = 1.0f;
+        }
+        c_hi *= tot_lo;
+        const float gam = tot_lo * __shfl_sync(full, x_hi, 31);  // all m decays
+        if (lane < m) {
+            nodes[lane] = node_lo;
+            coef[lane] = c_lo;
+        }
+        if (lane + 32 < m) {
+            nodes[lane + 32] = node_hi;
+            coef[lane + 32] = c_hi;
+        }
+        if (lane == 0) {
+            gam_s = gam;
+            m_s = m;
+        }
+    } else {
+        // warps 1-3: their share of the window copy, conv_hist[slot] <- win[accepted]
+        const int64_t total4 = int64_t(3) * a.C / 4;
+        const int64_t parts = int64_t(a.Hv) * CPH * (kApplyWarps - 1);
+        const int64_t per = (total4 + parts - 1) / parts;
+        const int64_t lo = ((int64_t(h) * CPH + q) * (kApplyWarps - 1) + warp - 1) * per, hi = min(total4, lo + per);
+        const float4 *wsrc = reinterpret_cast<const float4 *>(a.win + (int64_t(n0) + acc) * 3 * a.C);
+        float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(slot) * 3 * a.C);
+        for (int64_t i = lo + lane; i < hi; i += 32) hdst[i] = __ldg(wsrc + i);
     }
-    // one path step: k^_j (this lane's columns) and u_j (the warp's rows)
-    auto load_step = [&](int i, float4 &kv, float4 &ua, float4 &ub, float &cj) {
-        const int j = __shfl_sync(full, i < 32 ? node_lo : node_hi, i & 31);
-        cj = __shfl_sync(full, i < 32 ? c_lo : c_hi, i & 31);
-        const float *row = a.replay + ((int64_t(n0) + j) * a.Hv + h) * a.rstride;
-        kv = __ldg(reinterpret_cast<const float4 *>(row) + kc);
-        ua = __ldg(reinterpret_cast<const float4 *>(row + D + rbase));
-        ub = __ldg(reinterpret_cast<const float4 *>(row + D + rbase) + 1);
-    };
-    // root first: leaf-first entries m-1 .. 0, the next step's loads in flight
-    float4 kv, ua, ub, kn, un_a, un_b;
-    float cj, cn;
-    if (m > 0) load_step(m - 1, kv, ua, ub, cj);
-    for (int i = m - 1; i >= 0; --i) {
-        if (i > 0) load_step(i - 1, kn, un_a, un_b, cn);
-        const float uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+    __syncthreads();
+    const int m = m_s;
+    const float gam = gam_s;
+    if (has_rows) {
 #pragma unroll
         for (int f = 0; f < NF; ++f) {
-            // row rbase + ro + RI f
-            float uj = uw[RI * f];
-#pragma unroll
-            for (int qq = 1; qq < RI; ++qq)
-                if (ro == qq) uj = uw[RI * f + qq];
-            uj *= cj;
-            sv[f].x = fmaf(uj, kv.x, sv[f].x);
-            sv[f].y = fmaf(uj, kv.y, sv[f].y);
-            sv[f].z = fmaf(uj, kv.z, sv[f].z);
-            sv[f].w = fmaf(uj, kv.w, sv[f].w);
+            sv[f].x *= gam; sv[f].y *= gam; sv[f].z *= gam; sv[f].w *= gam;
         }
-        kv = kn; ua = un_a; ub = un_b; cj = cn;
     }
+    // root first: leaf-first entries m-1 .. 0, kBatch at a time
+    for (int top = m - 1; top >= 0; top -= kBatch) {
+        const int nb = min(kBatch, top + 1);  // entries top, top-1, .., top-nb+1 -> slots 0..nb-1
+        for (int x = tid; x < nb * DV4; x += kApplyWarps * 32) {
+            const int e = x / DV4, c = x % DV4;
+            kst[e][c] = __ldg(reinterpret_cast<const float4 *>(rbase_h + nodes[top - e] * rnode) + c);
+        }
+        for (int x = tid; x < nb * CR / 4; x += kApplyWarps * 32) {
+            const int e = x / (CR / 4), c = x % (CR / 4);
+            reinterpret_cast<float4 *>(ust[e])[c] =
+                __ldg(reinterpret_cast<const float4 *>(rbase_h + nodes[top - e] * rnode + D + rcta) + c);
+        }
+        __syncthreads();
+        if (has_rows) {
+            for (int e = 0; e < nb; ++e) {
+                const float cj = coef[top - e];
+                const float4 kv = kst[e][kc];
 #pragma unroll
-    for (int f = 0; f < NF; ++f)
-        *reinterpret_cast<float4 *>(sbase + (rbase + ro + RI * f) * D + 4 * kc) = sv[f];
-
+                for (int f = 0; f < NF; ++f) {
+                    // row rbase + ro + RI f
+                    const float uj = ust[e][rbase - rcta + ro + RI * f] * cj;
+                    sv[f].x = fmaf(uj, kv.x, sv[f].x);
+                    sv[f].y = fmaf(uj, kv.y, sv[f].y);
+                    sv[f].z = fmaf(uj, kv.z, sv[f].z);
+                    sv[f].w = fmaf(uj, kv.w, sv[f].w);
+                }
+            }
+        }
+        __syncthreads();  // the batch's staging may be overwritten
+    }
+    if (has_rows) {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            *reinterpret_cast<float4 *>(sbase + (rbase + ro + RI * f) * D + 4 * kc) = sv[f];
+    }
 }
 
 }  // namespace
@@ -232,16 +266,18 @@ extern "C" int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const i
     CommitArgs a{accepted, parents, node_off, slot_map, replay, replay_stride, win, ssm, conv_hist, status,
                  int(S), int(N), int(P), int(Hv), int(C), dims->max_seq_nodes};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    commit_preflight_kernel<<<unsigned((S + 7) / 8), 256, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_LAUNCH;
+    if (gdn::launch_pdl(commit_preflight_kernel, dim3(unsigned((S + 7) / 8)), dim3(256), 0, st, a) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
     // CTAs of 32 state rows: d / 32 per head (one for d = 16)
     const unsigned cph = unsigned((D + kCtaRows - 1) / kCtaRows);
     const dim3 grid{unsigned(Hv) * cph, unsigned(S)};
+    cudaError_t e;
+    const dim3 block(kApplyWarps * 32);
     switch (D) {
-        case 16: commit_apply_warp_kernel<16><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
-        case 32: commit_apply_warp_kernel<32><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
-        case 64: commit_apply_warp_kernel<64><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
-        default: commit_apply_warp_kernel<128><<<grid, kApplyWarps * 32, 0, st>>>(a); break;
+        case 16: e = gdn::launch_pdl(commit_apply_kernel<16>, grid, block, 0, st, a); break;
+        case 32: e = gdn::launch_pdl(commit_apply_kernel<32>, grid, block, 0, st, a); break;
+        case 64: e = gdn::launch_pdl(commit_apply_kernel<64>, grid, block, 0, st, a); break;
+        default: e = gdn::launch_pdl(commit_apply_kernel<128>, grid, block, 0, st, a); break;
     }
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }

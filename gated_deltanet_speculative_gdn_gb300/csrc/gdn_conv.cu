@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
     // (>= 0) or -1 - tap for history tap 0..2
     __shared__ int src[gdn::kMaxSeqNodes][3];
 
+    gdn::grid_dep_launch();
     if (tid == 0) {
         const int n0 = a.node_off[s], n1 = a.node_off[s + 1];
         int err = 0;
@@ -66,6 +67,9 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
         hdr[3] = slot;
     }
     __syncthreads();
+    // from here on: status, the conv history and the outputs, which the
+    // library's other kernels touch
+    gdn::grid_dep_wait();
     if (hdr[0]) {
         if (tid == 0) gdn::record_status(a.status, hdr[0]);
         return;
@@ -167,6 +171,8 @@ extern "C" int gdn_conv_tree_step(const gdn_dims *dims, const float *x, int64_t 
                int(S), int(N), int(P), int(C), dims->max_seq_nodes};
     const int c4 = int(C / 4);
     const dim3 grid{unsigned((c4 + kConvChannels / 4 - 1) / (kConvChannels / 4)), unsigned(S)};
-    conv_tree_step_kernel<<<grid, kConvThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return gdn::launch_pdl(conv_tree_step_kernel, grid, dim3(kConvThreads), 0, static_cast<cudaStream_t>(stream),
+                           a) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_LAUNCH;
 }

@@ -11,6 +11,33 @@
 
 namespace gdn {
 
+// Programmatic dependent launch.  The library's kernels run back to back on the
+// caller's stream with the programmatic-serialization attribute: each lets the
+// next one launch as soon as all its CTAs have started (launch_dependents), and
+// each waits, before it touches any buffer another kernel of the library may
+// write, for the previous grid to complete with its writes visible (wait; a
+// no-op when launched without the attribute).  Since every kernel waits, each
+// completed kernel implies all earlier ones completed.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `k` on `st` with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 // A bounded wait gives up after this long and reports GDN_DEV_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, s = blockIdx.y;
     const int kh = h / (a.Hv / a.Hk);
+    gdn::grid_dep_launch();
+    gdn::grid_dep_wait();  // xc, the state pool, status
 
     if (tid == 0) {
         const int n0 = a.node_off[s], n1 = a.node_off[s + 1];
@@ -559,6 +561,8 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int total = a.S * a.Hv;
     const int64_t C = a.C;
+    gdn::grid_dep_launch();
+    gdn::grid_dep_wait();  // xc, the state pool, status
 
     // ---- set-up: this CTA's valid items, barriers, tensor memory -------------
     if (warp == 0) {
@@ -1057,8 +1061,7 @@ int launch(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     const dim3 grid{unsigned(a.Hv), unsigned(a.S)};
-    k<<<grid, kThreads, L::BYTES, st>>>(map, a);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return gdn::launch_pdl(k, grid, dim3(kThreads), L::BYTES, st, map, a) == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 int sm_count() {
@@ -1095,8 +1098,9 @@ int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     if (sms <= 0) return GDN_ERR_LAUNCH;
     // one CTA per SM, each with at most kMaxItems items (more CTAs queue behind)
     int64_t grid = std::max<int64_t>(std::min<int64_t>(items, sms), (items + wsv::kMaxItems - 1) / wsv::kMaxItems);
-    k<<<unsigned(grid), wsv::kThreadsWS, wsv::BYTES, st>>>(map, xmap, a);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, a) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_LAUNCH;
 }
 
 // d = 128 with trees of up to 16 nodes: tensor cores; otherwise the FFMA kernel
