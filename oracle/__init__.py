@@ -4,9 +4,10 @@ Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg import this package.  The library under test never does.
 
 ``build()`` compiles ``gdn_oracle.c`` with gcc (-O2, -ffp-contract=off, no
-fast-math) into ``liboracle_gdn.so`` beside it.  ``build(mutant=k)`` builds a
-deliberately broken copy used only by the mutation test, which checks that
-every planted mistake fails at least one pin.
+fast-math) into ``liboracle_gdn.so`` beside it.  ``compile_source`` compiles
+another copy of the source the same way; the mutation test uses it to build
+deliberately broken copies and checks that every planted mistake fails at
+least one pin.
 """
 from __future__ import annotations
 
@@ -19,28 +20,27 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gdn_oracle.c")
+SOURCE = os.path.join(_HERE, "gdn_oracle.c")
+LIB = os.path.join(_HERE, "liboracle_gdn.so")
 
 OK, BAD_NODE_OFF, BAD_PARENT, BAD_SLOT, DUP_SLOT, BAD_ACCEPTED, BAD_DIMS, NOMEM = range(8)
 
 
-def lib_path(mutant: int = 0) -> str:
-    name = "liboracle_gdn.so" if mutant == 0 else f"liboracle_gdn_mutant{mutant}.so"
-    if mutant:
-        return os.path.join(_HERE, "_mutants", name)
-    return os.path.join(_HERE, name)
-
-
-def build(mutant: int = 0, force: bool = False) -> str:
-    out = lib_path(mutant)
-    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
-        return out
-    os.makedirs(os.path.dirname(out), exist_ok=True)
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 -ffp-contract=off (no fast-math) of one oracle source file into
+    a shared library at ``out``."""
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC",
-           "-shared", f"-DGDN_ORACLE_MUTANT={mutant}", "-o", out + ".tmp", _SRC, "-lm"]
+           "-shared", "-I", _HERE, "-o", out + ".tmp", src, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(out + ".tmp", out)
     return out
+
+
+def build(force: bool = False) -> str:
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= max(
+            os.path.getmtime(SOURCE), os.path.getmtime(os.path.join(_HERE, "gdn_oracle.h"))):
+        return LIB
+    return compile_source(SOURCE, LIB)
 
 
 class _Dims(ctypes.Structure):
@@ -83,9 +83,8 @@ def _i32(a) -> np.ndarray:
 
 
 class Oracle:
-    def __init__(self, mutant: int = 0):
-        path = build(mutant)
-        self.lib = ctypes.CDLL(path)
+    def __init__(self, lib_path: Optional[str] = None):
+        self.lib = ctypes.CDLL(lib_path or build())
         self.lib.gdn_oracle_conv_tree_step.argtypes = [
             ctypes.POINTER(_Dims), _P, ctypes.c_long, _P, _P, _P, _P, _P, _P, _P]
         self.lib.gdn_oracle_tree_verify.argtypes = [

@@ -40,10 +40,6 @@
 #include <stdlib.h>
 #include <string.h>
 
-#ifndef GDN_ORACLE_MUTANT
-#define GDN_ORACLE_MUTANT 0 /* != 0 only in the mutation test's builds */
-#endif
-
 #define L2_EPS 1e-6
 
 static double silu(double x) { return x / (1.0 + exp(-x)); }
@@ -108,28 +104,16 @@ int gdn_oracle_conv_tree_step(const gdn_oracle_dims *dm, const float *x, long x_
                 if (cur >= 0) {
                     col[b] = x + (size_t)(n0 + cur) * x_stride;
                 } else {
-#if GDN_ORACLE_MUTANT == 2
-                    col[b] = hist + (size_t)above * C;            /* newest taken as oldest */
-#else
                     col[b] = hist + (size_t)(K - 2 - above) * C;  /* h_{K-2} is the newest */
-#endif
                     ++above;
                 }
             }
             for (int c = 0; c < C; ++c) {
                 double acc = 0.0;
                 for (int j = 0; j < K; ++j) {       /* window tap j, oldest first */
-#if GDN_ORACLE_MUTANT == 1
-                    acc += (double)col[K - 1 - j][c] * (double)conv_w[(size_t)c * K + (K - 1 - j)];
-#else
                     acc += (double)col[K - 1 - j][c] * (double)conv_w[(size_t)c * K + j];
-#endif
                 }
-#if GDN_ORACLE_MUTANT == 13
-                xc[(size_t)(n0 + i) * C + c] = acc;
-#else
                 xc[(size_t)(n0 + i) * C + c] = silu(acc);
-#endif
                 for (int j = 0; j < K - 1; ++j)      /* commit window, oldest first */
                     win[((size_t)(n0 + i) * (K - 1) + j) * C + c] = col[K - 2 - j][c];
             }
@@ -181,83 +165,41 @@ int gdn_oracle_tree_verify(const gdn_oracle_dims *dm, const float *xc, const flo
         double *St = (double *)malloc(sizeof(double) * dd * (size_t)ns);
         if (!St) { rc = ORACLE_NOMEM; goto done; }
         for (int h = 0; h < Hv; ++h) {
-#if GDN_ORACLE_MUTANT == 6
-            const int kh = h % Hk;
-#else
             const int kh = h / G;                  /* [P3] q/k heads broadcast */
-#endif
             const float *S0f = ssm + ((size_t)slot * Hv + h) * dd;
             for (int r = 0; r < d; ++r)
                 for (int c = 0; c < d; ++c)
-#if GDN_ORACLE_MUTANT == 5
-                    S0[(size_t)r * d + c] = S0f[(size_t)c * d + r];
-#else
                     S0[(size_t)r * d + c] = S0f[(size_t)r * d + c];
-#endif
             for (int i = 0; i < ns; ++i) {
                 const int t = n0 + i, p = parents[t];
                 const float *row = xc + (size_t)t * C;
                 const float *q = row + (size_t)kh * d;
                 const float *k = row + (size_t)Hk * d + (size_t)kh * d;
                 const float *v = row + (size_t)2 * Hk * d + (size_t)h * d;
-#if GDN_ORACLE_MUTANT == 14
-                for (int c = 0; c < d; ++c) qn[c] = q[c];
-#else
                 l2_normalise(q, qn, d);
-#endif
-#if GDN_ORACLE_MUTANT == 8
-                for (int c = 0; c < d; ++c) kn[c] = k[c];
-#else
                 l2_normalise(k, kn, d);
-#endif
                 /* [P3] raw gates: beta = sigmoid(b), decay = exp(softplus(a + dt_bias) A) */
-#if GDN_ORACLE_MUTANT == 12
-                const double b = ba[(size_t)t * ba_stride + Hv + h];
-                const double a = ba[(size_t)t * ba_stride + h];
-#else
                 const double b = ba[(size_t)t * ba_stride + h];
                 const double a = ba[(size_t)t * ba_stride + Hv + h];
-#endif
                 const double beta = sigmoid(b);
-#if GDN_ORACLE_MUTANT == 9
-                const double decay = exp(softplus(a) * (double)A[h]);
-#else
                 const double decay = exp(softplus(a + (double)dt_bias[h]) * (double)A[h]);
-#endif
                 const double *Sp = p < 0 ? S0 : St + (size_t)p * dd;
                 double *S = St + (size_t)i * dd;
                 for (size_t e = 0; e < dd; ++e)
-#if GDN_ORACLE_MUTANT == 3
-                    S[e] = Sp[e];
-#else
                     S[e] = decay * Sp[e];                              /* S' */
-#endif
                 for (int r = 0; r < d; ++r) {
                     double sk = 0.0;
                     for (int c = 0; c < d; ++c) sk += S[(size_t)r * d + c] * kn[c];
-#if GDN_ORACLE_MUTANT == 4
-                    u[r] = beta * (sk - (double)v[r]);
-#else
                     u[r] = beta * ((double)v[r] - sk);
-#endif
                 }
                 double *orow = o + ((size_t)t * Hv + h) * d;
-#if GDN_ORACLE_MUTANT == 7
-                for (int r = 0; r < d; ++r) {
-                    double acc = 0.0;
-                    for (int c = 0; c < d; ++c) acc += S[(size_t)r * d + c] * qn[c];
-                    orow[r] = q_scale * acc;
-                }
-#endif
                 for (int r = 0; r < d; ++r)
                     for (int c = 0; c < d; ++c) S[(size_t)r * d + c] += u[r] * kn[c];
-#if GDN_ORACLE_MUTANT != 7
                 for (int r = 0; r < d; ++r) {
                     double acc = 0.0;
                     for (int c = 0; c < d; ++c) acc += S[(size_t)r * d + c] * qn[c];
                     orow[r] = q_scale * acc;
                 }
-#endif
                 double *rep = replay + ((size_t)t * Hv + h) * R;
                 for (int c = 0; c < d; ++c) rep[c] = kn[c];
                 for (int r = 0; r < d; ++r) rep[d + r] = u[r];
@@ -318,11 +260,7 @@ int gdn_oracle_commit(const gdn_oracle_dims *dm, const int *accepted, const int 
             float *Sf = ssm + ((size_t)slot * Hv + h) * dd;
             for (size_t e = 0; e < dd; ++e) S[e] = Sf[e];
             for (int step = 0; step < m; ++step) {
-#if GDN_ORACLE_MUTANT == 10
-                const int j = path[step];                   /* leaf first */
-#else
                 const int j = path[m - 1 - step];           /* root first */
-#endif
                 const double *rep = replay + ((size_t)(n0 + j) * Hv + h) * R;
                 const double *kn = rep, *u = rep + d, decay = rep[2 * d];
                 for (int r = 0; r < d; ++r)
@@ -331,11 +269,7 @@ int gdn_oracle_commit(const gdn_oracle_dims *dm, const int *accepted, const int 
             }
             for (size_t e = 0; e < dd; ++e) Sf[e] = (float)S[e];
         }
-#if GDN_ORACLE_MUTANT == 11
-        const int wnode = parents[n0 + a] >= 0 ? parents[n0 + a] : a;
-#else
         const int wnode = a;
-#endif
         const float *w = win + (size_t)(n0 + wnode) * (K - 1) * C;
         float *hst = conv_hist + (size_t)slot * (K - 1) * C;
         memcpy(hst, w, sizeof(float) * (size_t)(K - 1) * C);
