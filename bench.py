@@ -171,17 +171,17 @@ class DeviceWorkload:
     the two pools) are drawn on the device with torch's Philox generator keyed
     by the same stream keys, with the same distributions."""
 
-    def __init__(self, sp: W.Spec, rounds: int, device, seed_offset: int = 0):
+    def __init__(self, sp: W.Spec, rounds: int, device, seed_offset: int = 0, layer: int = 0):
         import torch
         self.sp, self.device = sp, device
         sh = sp.shape
         self.C = sh.conv_channels
         self.rs = (2 * sh.d + 1 + 3) // 4 * 4           # smallest replay row stride
-        lp = W.layer_params(sp, 0, with_pools=False)
+        lp = W.layer_params(sp, layer, with_pools=False)
         g = torch.Generator(device=device)
-        g.manual_seed(W.stream_key(sp.seed, seed_offset, W.TID_STATE) & ((1 << 63) - 1))
+        g.manual_seed(W.stream_key(sp.seed, seed_offset, layer, W.TID_STATE) & ((1 << 63) - 1))
         self.ssm = torch.randn((sh.n_slots, sh.h_v, sh.d, sh.d), generator=g, device=device) * 0.1
-        g.manual_seed(W.stream_key(sp.seed, seed_offset, W.TID_HIST) & ((1 << 63) - 1))
+        g.manual_seed(W.stream_key(sp.seed, seed_offset, layer, W.TID_HIST) & ((1 << 63) - 1))
         self.hist = torch.randn((sh.n_slots, 3, self.C), generator=g, device=device)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
         self.w, self.dt, self.A = t(lp.conv_w), t(lp.dt_bias), t(lp.A)
@@ -189,8 +189,8 @@ class DeviceWorkload:
         self.rounds = []
         self.host_rounds = []
         for r in range(rounds):
-            ri = W.round_inputs(sp, 0, r, with_x=False)
-            g.manual_seed(W.stream_key(sp.seed, seed_offset, W.TID_X, r) & ((1 << 63) - 1))
+            ri = W.round_inputs(sp, layer, r, with_x=False)
+            g.manual_seed(W.stream_key(sp.seed, seed_offset, layer, W.TID_X, r) & ((1 << 63) - 1))
             x = torch.randn((int(ri.node_off[-1]), self.C), generator=g, device=device)
             self.rounds.append(dict(x=x, ba=t(ri.ba), parents=t(ri.parents), node_off=t(ri.node_off),
                                     accepted=t(ri.accepted)))
@@ -346,10 +346,50 @@ def time_e2e(wl: DeviceWorkload, steps: int, warmup: int, host_rounds: int = 8):
     return {"ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def time_config(index: int, steps: int, warmup: int, device):
+    """The smaller workloads as whole steps: config 1 (a chain of 8), config 2
+    (four 16-node trees) and config 3 (the 48-layer stack: conv -> verify ->
+    commit per layer, each layer with its own weights and pools, timed as one
+    step over all layers)."""
+    import torch
+    sp = W.spec(index)
+    nr = min(sp.rounds, 4)
+    wls = [DeviceWorkload(sp, nr, device, layer=l) for l in range(sp.layers)]
+    flush = L2Flush(device)
+
+    def step(r):
+        for wl in wls:
+            wl.step(r % nr)
+
+    for i in range(warmup):
+        flush(i)
+        step(i)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(steps):
+        flush(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step(warmup + i)
+        b.record()
+        times.append((a, b))
+    torch.cuda.synchronize()
+    st = int(sum(int(wl.status.item()) != 0 for wl in wls))
+    assert st == 0, "device status set"
+    ms = statistics.mean(x.elapsed_time(y) for x, y in times)
+    hr = [wls[0].host_rounds[(warmup + i) % nr] for i in range(steps)]
+    byts = statistics.mean(sum(algo_bytes(sp, r.parents, r.node_off, r.accepted).values()) for r in hr) * sp.layers
+    nodes = wls[0].N * sp.layers
+    return {"workload": sp.name, "layers": sp.layers, "nodes_per_step": nodes, "ms_per_step": round(ms, 5),
+            "nodes_per_s": round(nodes / (ms * 1e-3), 1), "step_algo_gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+            "gpu_launches_per_step": 4 * sp.layers}
+
+
 # -------------------------------------------------------------- CPU baseline
-def oracle_sample(variant: str, budget_s: float = 12.0, seqs_per_step=None):
+def oracle_sample(variant: str, budget_s: float = 12.0, seqs_per_step=None, first_seq: int = 0, stride: int = 1):
     """Times the oracle (single-threaded C) on whole sequences of the sweep
-    workload until the budget is spent.  Returns (nodes, seconds, sequences)."""
+    workload (sequences first_seq, first_seq + stride, ...) until the budget is
+    spent.  Returns (nodes, seconds, sequences)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle as O
     orc = O.get()
@@ -358,7 +398,7 @@ def oracle_sample(variant: str, budget_s: float = 12.0, seqs_per_step=None):
     lp = W.layer_params(sp, 0, with_pools=False)
     nodes, secs, done = 0, 0.0, 0
     ri = W.round_inputs(sp, 0, 0)
-    s = 0
+    s = first_seq
     while True:
         sub = W.subset(sp, ri, [s % sh.n_seqs])
         n = int(sub.node_off[-1])
@@ -376,10 +416,88 @@ def oracle_sample(variant: str, budget_s: float = 12.0, seqs_per_step=None):
         assert rc == rc2 == rc3 == 0
         nodes += n
         done += 1
-        s += 1
+        s += stride
         if (seqs_per_step is not None and done >= seqs_per_step) or (seqs_per_step is None and secs >= budget_s):
             break
     return nodes, secs, done
+
+
+def _oracle_worker(args):
+    variant, budget_s, first, stride = args
+    return oracle_sample(variant, budget_s, first_seq=first, stride=stride)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_all_cores(variant: str, budget_s: float = 8.0):
+    """The oracle as independent per-sequence instances over every host core
+    (a spawned process pool; sequences are independent).  Returns (nodes,
+    seconds, sequences, cores): seconds is the longest worker's compute time."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle as O
+    O.build()                       # once, before the workers load it
+    n = host_cores()
+    with ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn")) as ex:
+        res = list(ex.map(_oracle_worker, [(variant, budget_s, w, n) for w in range(n)]))
+    return sum(r[0] for r in res), max(r[1] for r in res), sum(r[2] for r in res), n
+
+
+def parity_spot(wl: DeviceWorkload, seqs=(0, 63), r: int = 0):
+    """One more (untimed) step of the benchmark's own device-drawn round r,
+    checked against the oracle on a few sequences: the pools of their slots
+    are read before the step, the oracle runs conv -> verify -> commit on the
+    same inputs, and the outputs and committed state are compared."""
+    import torch
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle as O
+    sp, sh = wl.sp, wl.sp.shape
+    sm = W.slot_map(sp)
+    slots = [int(sm[s]) for s in seqs]
+    ssm0 = wl.ssm[slots].cpu().numpy()
+    hist0 = wl.hist[slots].cpu().numpy()
+    wl.status.zero_()
+    wl.step(r)
+    torch.cuda.synchronize()
+    ri = wl.host_rounds[r]
+    sub = W.subset(sp, ri, list(seqs))
+    rows = np.concatenate([np.arange(ri.node_off[s], ri.node_off[s + 1]) for s in seqs])
+    x = wl.rounds[r]["x"].cpu().numpy()[rows]
+    lp = W.layer_params(sp, 0, with_pools=False)
+    orc = O.get()
+    dm = O.Dims(len(seqs), len(rows), len(seqs), sh.h_k, sh.h_v, sh.d)
+    slot_ids = list(range(len(seqs)))
+    rc, xc, win = orc.conv_tree_step(dm, x, lp.conv_w, hist0, sub.parents, sub.node_off, slot_ids)
+    rc2, o, rep = orc.tree_verify(dm, xc.astype(np.float32), sub.ba, lp.dt_bias, lp.A, ssm0, sub.parents,
+                                  sub.node_off, slot_ids)
+    ssm1, hist1 = ssm0.copy(), hist0.copy()
+    rc3 = orc.commit(dm, sub.accepted, sub.parents, sub.node_off, slot_ids, rep, win, ssm1, hist1)
+    assert rc == rc2 == rc3 == 0
+
+    def rel(g, ref):
+        g, ref = np.asarray(g, np.float64), np.asarray(ref, np.float64)
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        return float(np.max(np.abs(g - ref) / np.maximum(np.abs(ref), 0.1 * rms)))
+
+    d = sh.d
+    g_rep = wl.replay.cpu().numpy()[rows, :, : 2 * d + 1]
+    acc = [int(a) >= 0 for a in sub.accepted]
+    out = {"sequences": list(seqs), "round": r, "status": int(wl.status.item()),
+           "xc": rel(wl.xc.cpu().numpy()[rows], xc), "o": rel(wl.o.cpu().numpy()[rows], o),
+           "replay_k": rel(g_rep[..., :d], rep[..., :d]), "replay_u": rel(g_rep[..., d:2 * d], rep[..., d:2 * d]),
+           "replay_decay": rel(g_rep[..., 2 * d], rep[..., 2 * d]),
+           "ssm": rel(wl.ssm[slots].cpu().numpy()[acc], ssm1[acc]) if any(acc) else 0.0,
+           "win_bit_exact": bool(np.array_equal(wl.win.cpu().numpy()[rows], win)),
+           "conv_hist_bit_exact": bool(np.array_equal(wl.hist[slots].cpu().numpy(), hist1))}
+    out["pass"] = bool(out["status"] == 0 and out["win_bit_exact"] and out["conv_hist_bit_exact"] and
+                       max(out[k] for k in ("xc", "o", "replay_k", "replay_u", "replay_decay", "ssm")) <= 1e-4)
+    return {k: (f"{v:.2e}" if isinstance(v, float) else v) for k, v in out.items()}
 
 
 # ---------------------------------------------------------------------- main

@@ -403,85 +403,105 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
 // Per (sequence, value head) "item" the contraction
 //     D[i][c] = sum_k S0[i][k] B[c][k],   B = [k_0..k_15 | q_0..q_15]   (raw rows)
 // is a 128 x 32 x 128 matrix product on tcgen05 with accumulators in tensor
-// memory, split so that it keeps fp32 accuracy (x = hi + lo, hi = x with the
-// low 13 mantissa bits cleared, lo exact):
-//     D = A_hi [B_hi | B_lo] + A_lo B_hi      (the dropped A_lo B_lo ~ 2^-22)
-// The first term is one tf32 product with N = 64 (B_hi and B_lo stacked).
-// The second, ~2^-11 of D, runs in fp16 (K = 16 per instruction) on 2^10 A_lo
-// (clear of fp16 subnormals), which costs it ~2^-12 of its own size; bf16's
-// 2^-9 is not enough, since the recurrence amplifies errors in S0 k.  A
-// tensor-core instruction takes about the same time for any N up to 256, so
-// this needs 24 instructions per item where three N = 32 tf32 products would
-// need 48.  The tensor cores read an fp32 operand as its hi part, so S0 and B
-// feed the hi operands unchanged.  The tensor cores align and truncate when
-// they accumulate, so the terms get short accumulators of their own, added in
-// fp32 by the epilogue.
+// memory.  Every operand is split as x = hi + lo, hi = x with the low 13
+// mantissa bits cleared (a tf32 number) and lo = x - hi (exact in fp32), and
+// all four products run as tf32:
+//     D = A_hi [B_hi | B_lo] + A_lo [B_hi | B_lo]
+// The tensor cores read an fp32 operand as its hi part, so S0 and the raw B
+// rows feed the hi operands unchanged and only the lo parts are written out
+// (as fp32).  tf32 keeps fp32's exponent range, so the split is exact at any
+// scale of the state or of q/k; the lo parts keep 11 bits, which puts the
+// product at ~2^-21 of fp32.  A tensor-core instruction costs about the same
+// for any N up to 256, so B_hi and B_lo always travel together as N = 64.
+// The tensor cores align and truncate when they accumulate, so the large
+// A_hi B_hi terms get one short accumulator per K-half and the small terms one
+// of their own; the epilogue adds them in fp32, smallest first.
 //
 // B holds the raw q/k rows, so the products start as soon as they land; the
-// epilogue scales column c by 1/|k_c| or 1/|q_c| (folded into Gamma_t), which
-// equals S0 k^ up to rounding.  The Gram terms of B with itself (k . k, q . k
-// and the norms) come from the tensor cores as well: 16 more tf32 products
-// (M = N = 64, B's rows [k | q | k_lo | q_lo] against themselves, so hi x hi,
-// hi x lo and lo x hi all appear).  The path coefficients then take a walk up
-// each node's ancestors that multiplies the decays.
+// epilogue scales column c by 1/|k_c| or 1/|q_c|, which equals S0 k^ up to
+// rounding.  The Gram terms of B with itself (k . k, q . k and the norms)
+// come from the tensor cores as well: M = N = 64 products of B's rows
+// [k | q | k_lo | q_lo] with themselves, so hi x hi, hi x lo, lo x hi and
+// lo x lo all appear.
+//
+// The tree is then solved in closed form.  With Ck[t][j] = gamma_{j->t}
+// k^_j . k^_t for j a strict ancestor of t and L = diag(beta) Ck, the node
+// updates u_t = beta_t (v_t - Gamma_t a_t - sum_j Ck[t][j] u_j) read
+//     (I + L) u = r,   r_t = beta_t (v_t - Gamma_t a_t)
+// so u = T r with T = (I + L)^-1, a unit lower-triangular 16 x 16 matrix that
+// is the same for all 128 state rows (the UT transform of the chunked delta
+// rule, restricted to the tree's ancestor pattern).  Likewise
+// o = q_scale (Gamma b + Cq u).  One warp forms T per item; every state row
+// then needs two small triangular matrix-vector products (u = T r, then
+// o from u) instead of a 16-step serial chain.
+//
+// Two measured properties of GB300 shape the pipeline.  A thread that issues
+// tcgen05.mma waits about 200 cycles per instruction whatever its shape,
+// while several issuing warps proceed side by side; so each kind of product
+// has an issuer warp of its own.  And a 16 KB S0 chunk arrives some 4 us after
+// its TMA load when every SM streams state, so each SM needs well over 100 KB
+// of loads in flight; so the lo part of a chunk is written over the chunk
+// itself once its A_hi products have read it, and shared memory goes to a
+// deep ring of S0 slots.
 //
 // One CTA per SM walks a list of items.  Warp roles:
 //   warp 0       TMA producer: S0 of each item as four 16 KB K-chunks
 //                ([128 rows][32 floats], 128-byte swizzle = the tensor cores'
-//                K-major operand layout) into a six-slot ring;
-//   warp 1       MMA issuer: per item, the Gram terms once its B is in; per
-//                chunk, A_hi [B_hi | B_lo] once the chunk lands, A_lo B_hi
-//                once its lo part is out;
-//   warps 2-3    splitters, items in order: B's lo part and fp16 copy as soon
-//                as the item's q/k rows land, then the lo part of every S0
-//                chunk as fp16 into a ring of two-chunk tiles, so S0 slots turn
-//                over at load speed;
+//                K-major operand layout) into a ring of NR slots;
+//   warps 1-3    MMA issuers, items and chunks in order: the Gram terms once
+//                the item's B is split (warp 1); A_hi [B_hi | B_lo] once a
+//                chunk lands (warp 2); A_lo [B_hi | B_lo] once the chunk holds
+//                its lo part, which frees the slot (warp 3);
 //   warps 4-7    team 0 and warps 8-11 team 1, on alternate items: the item's
 //                q/k rows by TMA into the team's B buffer (same layout as the
-//                chunks), gates, norms and path coefficients from the Gram
-//                terms, and the per-row epilogue reading the accumulators from
-//                tensor memory (thread i owns state row i).
-// A team's next q/k rows (loaded by the team) land while it runs the current
-// epilogue, and the S0 ring runs ahead of both teams, so loads, tensor-core
-// work and CUDA-core work of different items overlap.
+//                chunks), gates, the ancestor decays, norms and path
+//                coefficients from the Gram terms, T, and the per-row epilogue
+//                reading the accumulators from tensor memory (thread i owns
+//                state row i);
+//   warps 12-15  splitters, items in order: B's lo rows as soon as the item's
+//                q/k rows land, then the lo part of every S0 chunk, in place,
+//                as soon as its A_hi products are done.
+// A team's next q/k rows land while it runs the current epilogue, and the S0
+// ring runs ahead of both teams, so loads, tensor-core work and CUDA-core
+// work of different items overlap.
 namespace wsv {
 constexpr int D = 128;
-constexpr int kWarps = 12;
+constexpr int kWarps = 16;
 constexpr int kThreadsWS = kWarps * 32;
-constexpr int kSplit0 = 2, kSplitThreads = 64;     // splitter warps 2-3
+constexpr int kIssueGram = 1, kIssueHi = 2;       // MMA issuer warps (warp 3 issues the A_lo products)
 constexpr int kTeam0 = 4;                          // team t: warps 4 + 4t .. 7 + 4t
+constexpr int kSplit0 = 12, kSplitThreads = 128;   // splitter warps 12-15
 constexpr int kMaxItems = 64;                      // items per CTA
-constexpr int NR = 5;                              // S0 ring depth (K-chunks)
-constexpr int NLP = 2;                             // lo ring depth (two-chunk fp16 tiles)
+constexpr int NR = 9;                              // S0 ring depth (K-chunks)
+constexpr int kPrefetch = 2;                       // items whose state is requested into L2 ahead
 constexpr uint32_t kChunk = 128 * 128;             // one S0 K-chunk: 128 rows x 32 fp32
-constexpr uint32_t kLoTile = 128 * 128;            // S0 lo of two K-chunks: 128 rows x 64 fp16
-constexpr uint32_t kBChunk = 64 * 128;             // one B K-chunk: rows 0-31 hi, 32-63 lo (fp32)
-constexpr uint32_t kBTeam = 4 * kBChunk;           // one team's tf32 B
-constexpr uint32_t kGATile = 64 * 128;             // fp16 B of two K-chunks: 64 rows x 64 fp16
-constexpr uint32_t kGATeam = 2 * kGATile;          // one team's fp16 B: rows [k | q | k_lo | q_lo]
+constexpr uint32_t kBChunk = 64 * 128;             // one B K-chunk: rows 0-15 k, 16-31 q, 32-63 their lo
+constexpr uint32_t kBTeam = 4 * kBChunk;           // one team's B
 constexpr uint32_t kQKBox = 16 * 128;              // 16 rows of k or q, one K-chunk
 constexpr uint32_t RAW = 0;
-constexpr uint32_t LO = RAW + NR * kChunk;
-constexpr uint32_t BT = LO + NLP * kLoTile;        // per team: q/k rows normalised in place, lo below
-constexpr uint32_t GA = BT + 2 * kBTeam;           // per team
-constexpr uint32_t SMALL = GA + 2 * kGATeam;
-// per-team small area (4-byte words): the Gram terms as partial sums from the
-// four tensor-memory lane quarters, KA + KB = k_t . k_j and QA + QB = q_t . k_j
-// ([16][16]; the path coefficients ck, cq then overwrite KA, QA in place),
-// QQA + QQB = q_t . q_t, gates, parents, gsk, gsq = Gamma_t / |k_t|, Gamma_t / |q_t|
-constexpr int T_KA = 0, T_KB = 256, T_QA = 512, T_QB = 768, T_BETA = 1024, T_DEC = 1040, T_GSK = 1056,
-              T_PAR = 1072, T_GSQ = 1088, T_QQA = 1104, T_QQB = 1120, T_WORDS = 1136;
+constexpr uint32_t BT = RAW + NR * kChunk;         // per team
+constexpr uint32_t SMALL = BT + 2 * kBTeam;
+// per-team small area (4-byte words), [16][16] matrices:
+//   KA + KB = k_t . k_j and QA + QB = q_t . k_j (Gram partial sums from the
+//   hi and lo rows, row t); GM = gamma_{j->t} (row t; 1 on the diagonal, 0
+//   off the path); LNT = -L transposed (row j holds column j of -L, with
+//   L = beta_t Ck); CQT = q_scale Cq transposed (row j holds column j).
+//   QQA + QQB = q_t . q_t; gates, parents, Gamma_t / |k_t| (GSK),
+//   q_scale Gamma_t / |q_t| (GSQ), 1 / |k_t| (RK), Gamma_t (GAM).
+constexpr int T_KA = 0, T_KB = 256, T_QA = 512, T_QB = 768, T_GM = 1024, T_CQT = 1280, T_BETA = 1536,
+              T_DEC = 1552, T_GSK = 1568, T_PAR = 1584, T_GSQ = 1600, T_QQA = 1616, T_QQB = 1632,
+              T_RK = 1648, T_GAM = 1664, T_LNT = 1680, T_WORDS = 1936;
 // mbarriers
 constexpr int B_RFULL = 0;                 // NR: S0 chunk landed
-constexpr int B_REMPTY = B_RFULL + NR;     // NR: chunk split and its A_hi products done (64 + 1 arrivals)
-constexpr int B_LFULL = B_REMPTY + NR;     // 2 NLP, one per chunk half: lo part written (64)
-constexpr int B_LEMPTY = B_LFULL + 2 * NLP;  // NLP: the tile's A_lo products done (1)
-constexpr int B_QFULL = B_LEMPTY + NLP;    // per team: q/k rows landed (1 + bytes)
-constexpr int B_BREADY = B_QFULL + 2;      // per team: B split into lo and fp16 parts (64)
+constexpr int B_HDONE = B_RFULL + NR;      // NR: the chunk's A_hi products done (1)
+constexpr int B_LFULL = B_HDONE + NR;      // NR: its lo part written in place (64)
+constexpr int B_REMPTY = B_LFULL + NR;     // NR: the lo part's products done, slot free (1)
+constexpr int B_QFULL = B_REMPTY + NR;     // per team: q/k rows landed (1 + bytes)
+constexpr int B_BREADY = B_QFULL + 2;      // per team: B's lo rows written (128)
 constexpr int B_GFULL = B_BREADY + 2;      // per team: Gram terms complete (1)
-constexpr int B_ACCFULL = B_GFULL + 2;     // per team: accumulators complete (1)
+constexpr int B_ACCFULL = B_GFULL + 2;     // per team: accumulators complete (1 from each product issuer)
 constexpr int B_ACCEMPTY = B_ACCFULL + 2;  // per team: accumulators read (128)
-constexpr int B_DRAIN = B_ACCEMPTY + 2;    // the issuer's last tensor-core work done (1)
+constexpr int B_DRAIN = B_ACCEMPTY + 2;    // the issuers' last tensor-core work done (1 from each)
 constexpr int N_BARS = B_DRAIN + 1;
 constexpr int W_BARS = 2 * T_WORDS;
 constexpr int W_TMEM = W_BARS + 2 * N_BARS;
@@ -492,20 +512,15 @@ constexpr int SMALL_WORDS = W_LIST + 4 * kMaxItems;
 constexpr size_t BYTES = SMALL + SMALL_WORDS * 4 + 1024;
 static_assert(BYTES <= 227 * 1024, "shared memory");
 static_assert((W_BARS % 2) == 0, "mbarriers are 8-byte aligned");
-// instruction descriptors: fp32 accumulate, K-major operands, M = 128;
-// tf32 x tf32 with N = 64 and fp16 x fp16 with N = 32
+static_assert((T_WORDS % 4) == 0 && (T_GM % 4) == 0 && (T_CQT % 4) == 0, "float4 rows");
+// instruction descriptors: fp32 accumulate, tf32 x tf32, K-major operands;
+// M = 128, N = 64 for the contraction and M = N = 64 for the Gram terms
 constexpr uint32_t IDESC_TF32 = (1u << 4) | (2u << 7) | (2u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t IDESC_F16 = (1u << 4) | (0u << 7) | (0u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-// the Gram terms: fp16, M = 64, N = 64, both operands the team's fp16 B
-constexpr uint32_t IDESC_GRAM = (1u << 4) | (0u << 7) | (0u << 10) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
-constexpr float kLoScale = 1024.0f;                // A_lo is stored as fp16(2^10 A_lo)
-// the fp16 B holds hi = fp16(2^-8 x) (range up to ~1.7e7) and lo =
-// fp16(2^11 (2^-8 x - hi)), so x = 2^8 (hi + 2^-11 lo) to ~2^-22
-constexpr float kBScale = 1.0f / 256.0f, kBLoScale = 2048.0f;
+constexpr uint32_t IDESC_GRAM = (1u << 4) | (2u << 7) | (2u << 10) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
 // Team t's accumulators start at column 256 t: K-half kh (chunks 2 kh, 2 kh + 1)
 // owns columns 64 kh .. 64 kh + 63, A_hi B_hi in the first 32 and A_hi B_lo in
-// the last 32; 2^10 A_lo 2^-8 B_hi of all four K-chunks sits at 128.  The
-// Gram terms G of the fp16 B with itself (M = 64: row a of G in lane
+// the last 32; A_lo B_hi and A_lo B_lo of all four K-chunks sit at 128 and 160.
+// The Gram terms G of B's 64 rows with themselves (M = 64: row a of G in lane
 // 32 (a / 16) + a % 16) sit at 192.
 constexpr uint32_t TMEM_COLS = 512, TEAM_COLS = 256, LHCOL = 128, GCOL = 192;
 
@@ -527,20 +542,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gdn::smem_addr(bar)) : "memory");
 }
+// x - (x with the low 13 mantissa bits cleared), exact
 __device__ __forceinline__ float4 lo4(float4 x) {
     return make_float4(x.x - gdn::tf32_hi(x.x), x.y - gdn::tf32_hi(x.y), x.z - gdn::tf32_hi(x.z),
                        x.w - gdn::tf32_hi(x.w));
-}
-// -(x with the low 13 mantissa bits cleared)
-__device__ __forceinline__ float neg_hi(float x) { return __uint_as_float((__float_as_uint(x) & 0xFFFFE000u) ^ 0x80000000u); }
-__device__ __forceinline__ uint2 f16x4(float4 x) {
-    return make_uint2(gdn::pack_f16x2(x.x, x.y), gdn::pack_f16x2(x.z, x.w));
-}
-// Byte offset of 16-bit elements k..k+3 (k % 4 == 0) of row `row` in a K-major
-// operand of 64 elements per row in the 128-byte swizzle (tile k >> 6).
-__device__ __forceinline__ uint32_t sw_off_h(int row, int k, uint32_t tile) {
-    return uint32_t(k >> 6) * tile + uint32_t(row) * 128u + ((uint32_t(((k & 63) >> 3) ^ (row & 7))) << 4) +
-           uint32_t((k >> 2) & 1) * 8u;
 }
 }  // namespace wsv
 
@@ -560,7 +565,6 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int total = a.S * a.Hv;
-    const int64_t C = a.C;
     gdn::grid_dep_launch();
     gdn::grid_dep_wait();  // xc, the state pool, status
 
@@ -593,10 +597,11 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t count = 1;
-            if (i >= B_REMPTY && i < B_REMPTY + NR) count = kSplitThreads + 1;
-            if (i >= B_LFULL && i < B_LFULL + 2 * NLP) count = kSplitThreads;
-            if (i >= B_BREADY && i < B_BREADY + 2) count = kSplitThreads;
+            if (i >= B_LFULL && i < B_LFULL + NR) count = kSplitThreads;
+            if (i >= B_BREADY && i < B_BREADY + 2) count = 128;
             if (i >= B_ACCEMPTY && i < B_ACCEMPTY + 2) count = 128;
+            if (i >= B_ACCFULL && i < B_ACCFULL + 2) count = 2;
+            if (i == B_DRAIN) count = 3;
             gdn::mbar_init(bars + i, count);
         }
         gdn::fence_mbar_init();
@@ -616,10 +621,20 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     if (warp == 0) {
         // ---- producer: S0 chunks in order into the ring ----------------------
         if (lane == 0) {
+            // the ring holds little more than one item, so the states of the
+            // next kPrefetch items are requested into L2 ahead of their loads
+            auto prefetch_item = [&](int v) {
+                if (v >= nv) return;
+                const int4 e = list[v];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) gdn::tma_prefetch_2d(&tmap, 32 * c, (e.w * a.Hv + e.x % a.Hv) * D);
+            };
+            for (int v = 1; v <= kPrefetch; ++v) prefetch_item(v);
             int g = 0;
             for (; g < nchunks; ++g) {
                 const int r = g % NR;
                 if (g >= NR && !wait_or_abort(bars + B_REMPTY + r, uint32_t((g / NR - 1) & 1), abort_flag)) break;
+                if ((g & 3) == 0) prefetch_item((g >> 2) + kPrefetch + 1);
                 const int4 e = list[g >> 2];
                 uint64_t *fb = bars + B_RFULL + r;
                 gdn::mbar_arrive_expect_tx(fb, kChunk);
@@ -633,149 +648,104 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---- MMA issuer: items and chunks in order -----------------------------
+    } else if (warp < kTeam0) {
+        // ---- MMA issuers, items and chunks in order.  A thread waits about 200
+        //      cycles on each tcgen05.mma it issues, whatever its shape, while
+        //      several issuing warps proceed side by side, so the three kinds of
+        //      product have a warp each: the Gram terms, A_hi [B_hi | B_lo] (which
+        //      frees S0 slots) and A_lo [B_hi | B_lo] (which frees lo slots). -------
         if (lane == 0) {
             bool ok = true;
             for (int v = 0; v < nv && ok; ++v) {
                 const int t = v & 1, ut = v >> 1;
                 if (!wait_or_abort(bars + B_BREADY + t, uint32_t(ut & 1), abort_flag)) break;
                 if (ut > 0 && !wait_or_abort(bars + B_ACCEMPTY + t, uint32_t((ut - 1) & 1), abort_flag)) break;
+                gdn::tc_fence_after_sync();
                 const uint32_t dacc = tmem + TEAM_COLS * t;
-                const uint32_t bt0 = sbase + BT + t * kBTeam, ga0 = sbase + GA + t * kGATeam;
-                // Gram terms of the fp16 B's 64 rows [k | q | k_lo | q_lo] with
-                // themselves: hi x hi, hi x lo and lo x hi all appear in the one product
-                for (int kt = 0; kt < 2; ++kt) {
-                    uint64_t gd = gdn::desc_sw128(ga0 + kt * kGATile);
+                const uint32_t bt0 = sbase + BT + t * kBTeam;
+                if (warp == kIssueGram) {
+                    // Gram terms of B's 64 rows [k | q | k_lo | q_lo] with themselves
+                    for (int kt = 0; kt < 4; ++kt) {
+                        uint64_t gd = gdn::desc_sw128(bt0 + kt * kBChunk);
+                        // a K-step (8 tf32) is 32 bytes: 2 in the descriptors' address field
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks, gd += 2)
-                        gdn::mma_f16(dacc + GCOL, gd, gd, IDESC_GRAM, (kt | ks) != 0);
+                        for (int ks = 0; ks < 4; ++ks, gd += 2)
+                            gdn::mma_tf32(dacc + GCOL, gd, gd, IDESC_GRAM, (kt | ks) != 0);
+                    }
+                    gdn::mma_commit(bars + B_GFULL + t);
+                    continue;
                 }
-                gdn::mma_commit(bars + B_GFULL + t);
                 for (int kb = 0; kb < 4; ++kb) {
-                    const int g = 4 * v + kb, r = g % NR, q = g % (2 * NLP), l = (g >> 1) % NLP;
-                    if (!wait_or_abort(bars + B_RFULL + r, uint32_t((g / NR) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    gdn::tc_fence_after_sync();
-                    const uint32_t dk = dacc + 64u * (kb >> 1);
-                    uint64_t ahi = gdn::desc_sw128(sbase + RAW + r * kChunk);
+                    const int g = 4 * v + kb;
                     uint64_t bst = gdn::desc_sw128(bt0 + kb * kBChunk);  // [B_hi | B_lo], 64 rows
-                    // a K-step (8 tf32 or 16 fp16) is 32 bytes: 2 in the descriptors' address field
+                    const int r = g % NR;
+                    const uint32_t par = uint32_t((g / NR) & 1);
+                    uint64_t a_op = gdn::desc_sw128(sbase + RAW + r * kChunk);
+                    if (warp == kIssueHi) {
+                        // the raw chunk (read as A_hi); then the splitters may
+                        // overwrite it with its lo part
+                        if (!wait_or_abort(bars + B_RFULL + r, par, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        gdn::tc_fence_after_sync();
+                        const uint32_t dk = dacc + 64u * (kb >> 1);
 #pragma unroll 1
-                    for (int ks = 0; ks < 4; ++ks, ahi += 2, bst += 2)
-                        gdn::mma_tf32(dk, ahi, bst, IDESC_TF32, ((kb & 1) | ks) != 0);
-                    gdn::mma_commit(bars + B_REMPTY + r);
-                    if (!wait_or_abort(bars + B_LFULL + q, uint32_t((g / (2 * NLP)) & 1), abort_flag)) {
-                        ok = false;
-                        break;
+                        for (int ks = 0; ks < 4; ++ks, a_op += 2, bst += 2)
+                            gdn::mma_tf32(dk, a_op, bst, IDESC_TF32, ((kb & 1) | ks) != 0);
+                        gdn::mma_commit(bars + B_HDONE + r);
+                    } else {
+                        // the same slot once it holds the lo part; then it is free
+                        if (!wait_or_abort(bars + B_LFULL + r, par, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        gdn::tc_fence_after_sync();
+#pragma unroll 1
+                        for (int ks = 0; ks < 4; ++ks, a_op += 2, bst += 2)
+                            gdn::mma_tf32(dacc + LHCOL, a_op, bst, IDESC_TF32, (kb | ks) != 0);
+                        gdn::mma_commit(bars + B_REMPTY + r);
                     }
-                    gdn::tc_fence_after_sync();
-                    // this chunk's 32 K-columns are the (kb & 1) half of the two-chunk tiles
-                    uint64_t alo = gdn::desc_sw128(sbase + LO + l * kLoTile + 64u * (kb & 1));
-                    uint64_t bh = gdn::desc_sw128(ga0 + (kb >> 1) * kGATile + 64u * (kb & 1));  // rows 0-31
-#pragma unroll 1
-                    for (int ks = 0; ks < 2; ++ks, alo += 2, bh += 2)
-                        gdn::mma_f16(dacc + LHCOL, alo, bh, IDESC_F16, (kb | ks) != 0);
-                    if (g & 1) gdn::mma_commit(bars + B_LEMPTY + l);
                 }
                 if (ok) gdn::mma_commit(bars + B_ACCFULL + t);
             }
-            // every tensor-core operation of this thread completes before the
+            // every tensor-core operation of these threads completes before the
             // tensor memory is released
             gdn::mma_commit(bars + B_DRAIN);
             gdn::mbar_wait_bounded(bars + B_DRAIN, 0);
         }
-    } else if (warp < kTeam0) {
-        // ---- splitters, items in order: the lo and fp16 parts of the item's raw
-        //      q/k rows (B), then 2^10 (x - hi) of each S0 chunk as fp16.  Chunk g
-        //      fills half g & 1 of lo tile (g / 2) % NLP. ----------------------------
+    } else if (warp >= kSplit0) {
+        // ---- splitters, chunks in order: once a chunk's A_hi products have read
+        //      it, each 16-byte unit is replaced by its lo part (an elementwise
+        //      pass in the chunk's own swizzled layout). -------------------------
         const int st = tid - kSplit0 * 32;
-        // S0 chunks: thread st takes rows rg + 8 j (j < 16) at 16-byte unit u, which
-        // holds K-columns k .. k + 3 (the swizzle phase of those rows is rg).  A
-        // warp's four rows rg cover both bank halves of the fp16 tile.  The fp16
-        // lo goes to byte dst0 (first half of a tile) or dst1 (second half), plus
-        // 1024 j.
-        const int sl = st & 31, u = sl & 7;
-        const int rg = ((sl >> 3) & 1) | ((st >> 5) << 1) | (((sl >> 4) & 1) << 2);
-        const int k = 4 * (u ^ rg);
-        const uint32_t src = uint32_t(rg) * 128u + uint32_t(u) * 16u;
-        const uint32_t dst0 = uint32_t(rg) * 128u + (uint32_t((k >> 3) ^ rg) << 4) + uint32_t((k >> 2) & 1) * 8u;
-        const uint32_t dst1 = uint32_t(rg) * 128u + (uint32_t(((32 + k) >> 3) ^ rg) << 4) + uint32_t((k >> 2) & 1) * 8u;
-        const uint64_t scale = gdn::f2pack(kLoScale, kLoScale);
-        bool ok = true;
-        for (int v = 0; v < nv && ok; ++v) {
-            const int t = v & 1;
-            // B: rows c (k of node c, then q of node c - 16) of each K-chunk; tf32
-            // lo below them (rows 32 + c, same swizzle phase); the fp16 B beside
-            if (!wait_or_abort(bars + B_QFULL + t, uint32_t((v >> 1) & 1), abort_flag)) break;
-            {
-                unsigned char *bt = sb + BT + t * kBTeam, *ga = sb + GA + t * kGATeam;
-#pragma unroll 4
-                for (int j = 0; j < 16; ++j) {
-                    const int kb = j >> 2, c = (st >> 3) + 8 * (j & 3), uu = st & 7;
-                    unsigned char *p = bt + kb * kBChunk + c * 128 + uu * 16;
-                    const float4 x = *reinterpret_cast<const float4 *>(p);
-                    *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
-                    // fp16 hi of 2^-8 x, and 2^11 times what it misses (exact before rounding)
-                    const int kk = 32 * kb + 4 * (uu ^ (c & 7));
-                    const float4 y = scale4(x, kBScale);
-                    const uint2 hh = f16x4(y);
-                    const float2 h01 = gdn::unpack_f16x2(hh.x), h23 = gdn::unpack_f16x2(hh.y);
-                    const float4 r = make_float4((y.x - h01.x) * kBLoScale, (y.y - h01.y) * kBLoScale,
-                                                 (y.z - h23.x) * kBLoScale, (y.w - h23.y) * kBLoScale);
-                    *reinterpret_cast<uint2 *>(ga + sw_off_h(c, kk, kGATile)) = hh;
-                    *reinterpret_cast<uint2 *>(ga + sw_off_h(32 + c, kk, kGATile)) = f16x4(r);
-                }
-                gdn::fence_proxy_async_smem();
-                mbar_arrive(bars + B_BREADY + t);
+        for (int g = 0; g < nchunks; ++g) {
+            const int r = g % NR;
+            if (!wait_or_abort(bars + B_HDONE + r, uint32_t((g / NR) & 1), abort_flag)) break;
+            float4 *c = reinterpret_cast<float4 *>(sb + RAW + r * kChunk);
+            constexpr int kPer = int(kChunk / 16) / kSplitThreads;  // 16-byte units per thread
+#pragma unroll
+            for (int b = 0; b < kPer; b += kPer / 2) {
+                float4 x[kPer / 2];
+#pragma unroll
+                for (int j = 0; j < kPer / 2; ++j) x[j] = c[st + kSplitThreads * (b + j)];
+#pragma unroll
+                for (int j = 0; j < kPer / 2; ++j) c[st + kSplitThreads * (b + j)] = lo4(x[j]);
             }
-            for (int kb = 0; kb < 4; ++kb) {
-                const int g = 4 * v + kb, r = g % NR, pi = g >> 1, l = pi % NLP;
-                if (!wait_or_abort(bars + B_RFULL + r, uint32_t((g / NR) & 1), abort_flag) ||
-                    (!(g & 1) && pi >= NLP &&
-                     !wait_or_abort(bars + B_LEMPTY + l, uint32_t((pi / NLP - 1) & 1), abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                const unsigned char *raw = sb + RAW + r * kChunk + src;
-                unsigned char *lo = sb + LO + l * kLoTile + ((g & 1) ? dst1 : dst0);
-                constexpr int kPer = int(kChunk / 16) / kSplitThreads;  // 16 float4 per thread, in two batches
-#pragma unroll
-                for (int b = 0; b < kPer; b += kPer / 2) {
-                    float4 x[kPer / 2];
-#pragma unroll
-                    for (int j = 0; j < kPer / 2; ++j) x[j] = *reinterpret_cast<const float4 *>(raw + 1024 * (b + j));
-#pragma unroll
-                    for (int j = 0; j < kPer / 2; ++j) {
-                        // 2^10 (x - hi): x plus hi with its sign flipped is exact, and so is the scaling
-                        const uint64_t lo01 = gdn::mul2(
-                            gdn::add2(gdn::f2pack(x[j].x, x[j].y), gdn::f2pack(neg_hi(x[j].x), neg_hi(x[j].y))), scale);
-                        const uint64_t lo23 = gdn::mul2(
-                            gdn::add2(gdn::f2pack(x[j].z, x[j].w), gdn::f2pack(neg_hi(x[j].z), neg_hi(x[j].w))), scale);
-                        const float2 fa = gdn::f2unpack(lo01), fb = gdn::f2unpack(lo23);
-                        *reinterpret_cast<uint2 *>(lo + 1024 * (b + j)) =
-                            make_uint2(gdn::pack_f16x2(fa.x, fa.y), gdn::pack_f16x2(fb.x, fb.y));
-                    }
-                }
-                gdn::fence_proxy_async_smem();
-                mbar_arrive(bars + B_REMPTY + r);
-                mbar_arrive(bars + B_LFULL + g % (2 * NLP));
-            }
+            gdn::fence_proxy_async_smem();
+            mbar_arrive(bars + B_LFULL + r);
         }
     } else {
         // ---- math teams ----------------------------------------------------------
         const int team = (warp - kTeam0) >> 2, tw = warp & 3;  // warp within the team = its TMEM lane quarter
         const int ttid = tw * 32 + lane;                       // 0..127
         const int row = ttid;                                  // tensor-memory lane = state row
-        int *tws = words + team * T_WORDS;
-        float *ka = reinterpret_cast<float *>(tws + T_KA), *kb = reinterpret_cast<float *>(tws + T_KB);
-        float *qa = reinterpret_cast<float *>(tws + T_QA), *qb = reinterpret_cast<float *>(tws + T_QB);
-        float *qqa = reinterpret_cast<float *>(tws + T_QQA), *qqb = reinterpret_cast<float *>(tws + T_QQB);
-        float *beta_s = reinterpret_cast<float *>(tws + T_BETA), *dec_s = reinterpret_cast<float *>(tws + T_DEC);
-        float *gsk = reinterpret_cast<float *>(tws + T_GSK), *gsq = reinterpret_cast<float *>(tws + T_GSQ);
-        int *par = tws + T_PAR;
+        float *tws = reinterpret_cast<float *>(words + team * T_WORDS);
+        float *ka = tws + T_KA, *kb = tws + T_KB, *qa = tws + T_QA, *qb = tws + T_QB;
+        float *gm = tws + T_GM, *cqt = tws + T_CQT, *lnt = tws + T_LNT;
+        float *qqa = tws + T_QQA, *qqb = tws + T_QQB, *beta_s = tws + T_BETA, *dec_s = tws + T_DEC;
+        float *gsk = tws + T_GSK, *gsq = tws + T_GSQ, *rk_s = tws + T_RK, *gam_s = tws + T_GAM;
+        int *par = reinterpret_cast<int *>(tws + T_PAR);
         unsigned char *bt_t = sb + BT + team * kBTeam;
 
         // parents and gate inputs of the team's next item, loaded one item ahead
@@ -796,23 +766,42 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         };
         prefetch(team);
         // one thread of the team loads an item's raw q/k rows into the team's B
-        // (rows n0 .. n0 + 15; rows past the last node are another sequence's or
-        // zero-filled past the tensor, and the team zeroes them)
+        // and its v rows into the team's v tile (rows n0 .. n0 + 15; rows past
+        // the sequence's last node belong to the next sequence, or are
+        // zero-filled past the tensor: they only feed outputs that are never
+        // written)
         int qk_issued = 0;
         auto issue_qk = [&](int v) {
             if (ttid != 0 || v >= nv) return;
             const int4 e = list[v];
             const int h = e.x % a.Hv, kh = h / (a.Hv / a.Hk);
-            uint64_t *qb = bars + B_QFULL + team;
-            gdn::mbar_arrive_expect_tx(qb, 8 * kQKBox);
+            uint64_t *qbar = bars + B_QFULL + team;
+            gdn::mbar_arrive_expect_tx(qbar, 8 * kQKBox);
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) {
-                gdn::tma_load_2d(bt_t + kb * kBChunk, &xmap, a.Hk * D + kh * D + 32 * kb, e.y, qb);
-                gdn::tma_load_2d(bt_t + kb * kBChunk + kQKBox, &xmap, kh * D + 32 * kb, e.y, qb);
+            for (int c = 0; c < 4; ++c) {
+                gdn::tma_load_2d(bt_t + c * kBChunk, &xmap, a.Hk * D + kh * D + 32 * c, e.y, qbar);
+                gdn::tma_load_2d(bt_t + c * kBChunk + kQKBox, &xmap, kh * D + 32 * c, e.y, qbar);
             }
             ++qk_issued;
         };
         issue_qk(team);
+        // the team writes the lo rows of its next item's B as soon as the rows
+        // land (the Gram and product issuers wait for them)
+        auto split_b = [&](int v) -> bool {
+            if (v >= nv) return false;
+            if (!wait_or_abort(bars + B_QFULL + team, uint32_t((v >> 1) & 1), abort_flag)) return false;
+#pragma unroll
+            for (int j = 0; j < (4 * 32 * 8) / 128; ++j) {
+                const int idx = ttid + 128 * j;  // 16-byte unit: K-chunk idx / 256, rows 0-31
+                unsigned char *p = bt_t + (idx >> 8) * kBChunk + (idx & 255) * 16;
+                const float4 x = *reinterpret_cast<const float4 *>(p);
+                *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
+            }
+            gdn::fence_proxy_async_smem();
+            mbar_arrive(bars + B_BREADY + team);
+            return true;
+        };
+        bool staged_nx = split_b(team);
 
         for (int v = team; v < nv; v += 2) {
             const int ut = v >> 1;
@@ -824,28 +813,53 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             // the team's previous epilogue has finished reading the small area
             team_sync(team);
 
-            // ---- A: parents and gates ---------------------------------------------
-            if (ttid < lc) {
-                if (p < -1 || p >= ttid) {
+            // ---- A: parents and gates (warp 0 of the team: lane = node) -----------
+            if (ttid < kSeg) {
+                if (ttid < lc && (p < -1 || p >= ttid)) {
                     gdn::record_status(a.status, GDN_DEV_BAD_PARENT);
                     p = -1;  // outputs of a failed call are unspecified; keep the walks in bounds
                 }
-                par[ttid] = p;
+                par[ttid] = ttid < lc ? p : -1;
             }
-            if (tw == 0 && lane < lc) {
-                const int64_t n = n0 + lane;
-                const float dec = expf(gdn::softplus_f(av + dtb) * Ah);
-                beta_s[lane] = gdn::sigmoid_f(bv);
+            if (tw == 0 && lane < kSeg) {
+                float dec = 1.f, bet = 0.f;
+                if (lane < lc) {
+                    dec = expf(gdn::softplus_f(av + dtb) * Ah);
+                    bet = gdn::sigmoid_f(bv);
+                    a.replay[((n0 + lane) * int64_t(a.Hv) + h) * a.rstride + 2 * D] = dec;
+                }
+                beta_s[lane] = bet;
                 dec_s[lane] = dec;
-                a.replay[(n * a.Hv + h) * a.rstride + 2 * D] = dec;
             }
+            __syncwarp();
+            // ---- the ancestor decays: lane t walks its path and writes row t of
+            //      GM, gamma_{j->t} = the decays strictly after j up to t (1 on the
+            //      diagonal, 0 off the path), and Gamma_t, all the decays on it.
+            //      Products along the path only, so underflow can only drop terms
+            //      that are already below the float range. ------------------------
+            if (tw == 0 && lane < kSeg) {
+                float4 *g4 = reinterpret_cast<float4 *>(gm + lane * kSeg);
+#pragma unroll
+                for (int j4 = 0; j4 < kSeg / 4; ++j4) g4[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                float g = 0.f;
+                if (lane < lc) {
+                    gm[lane * kSeg + lane] = 1.f;
+                    g = 1.f;
+                    for (int cur = lane;;) {
+                        g *= dec_s[cur];
+                        cur = par[cur];
+                        if (cur < 0) break;
+                        gm[lane * kSeg + cur] = g;
+                    }
+                }
+                gam_s[lane] = g;
+            }
+
             // ---- B: Gram terms from tensor memory.  Warp tw holds G rows 16 tw ..
-            //      16 tw + 15 in lanes 0..15, row and column index a = [k | q | k_lo |
-            //      q_lo] of the fp16 B: KA, QA take hi x hi + 2^-11 hi x lo (columns
-            //      j and 32 + j), KB, QB take 2^-11 lo x hi (column j), all times
-            //      2^16 (the 2^-8 scale of both sides); QQA, QQB the same for
-            //      q_t . q_t. ----------------------------------------------------------
-            const bool staged = wait_or_abort(bars + B_QFULL + team, uint32_t(ut & 1), abort_flag);
+            //      16 tw + 15 (k, q, k_lo, q_lo of the nodes) in lanes 0..15, columns
+            //      [k | q | k_lo | q_lo]: a row against column j plus column 32 + j is
+            //      its dot product with all of k_j. ----------------------------------
+            const bool staged = staged_nx;
             // warp-uniform: tcgen05.ld is warp-collective
             const bool gready =
                 __all_sync(0xffffffffu, staged && wait_or_abort(bars + B_GFULL + team, uint32_t(ut & 1), abort_flag));
@@ -856,95 +870,66 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 gdn::tmem_ld32(grow, d0);
                 gdn::tmem_ld32(grow + 32u, d1);
                 if (lane < kSeg) {
-                    const bool hi = tw < 2;
-                    // 2^16 undoes the 2^-8 scale on both sides; 2^-11 the lo scale
-                    constexpr float kG = 1.0f / (kBScale * kBScale), kX = 1.0f / kBLoScale, kGX = kG * kX;
                     float *dst = (tw == 0 ? ka : tw == 1 ? qa : tw == 2 ? kb : qb) + lane * kSeg;
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
                         const int j = 4 * j4;
                         *reinterpret_cast<float4 *>(dst + j) =
-                            hi ? make_float4(kG * fmaf(d1[j], kX, d0[j]), kG * fmaf(d1[j + 1], kX, d0[j + 1]),
-                                             kG * fmaf(d1[j + 2], kX, d0[j + 2]), kG * fmaf(d1[j + 3], kX, d0[j + 3]))
-                               : make_float4(kGX * d0[j], kGX * d0[j + 1], kGX * d0[j + 2], kGX * d0[j + 3]);
+                            make_float4(d0[j] + d1[j], d0[j + 1] + d1[j + 1], d0[j + 2] + d1[j + 2], d0[j + 3] + d1[j + 3]);
                     }
                     if (tw & 1) {
+                        // q_t . q_t: columns 16 + t and 48 + t (no dynamic register index)
                         float qq = 0.f;
 #pragma unroll
                         for (int b = 0; b < kSeg; ++b)
-                            if (b == lane) qq = hi ? kG * fmaf(d1[kSeg + b], kX, d0[kSeg + b]) : kGX * d0[kSeg + b];
-                        (hi ? qqa : qqb)[lane] = qq;
+                            if (b == lane) qq = d0[kSeg + b] + d1[kSeg + b];
+                        (tw == 1 ? qqa : qqb)[lane] = qq;
                     }
                 }
             }
-            team_sync(team);  // Gram terms, parents and decays of every node are in
+            team_sync(team);  // Gram terms, parents, decays and GM are in
 
-            // ---- C: path coefficients.  For node t and j on its path (j != t):
-            //      ck[t][j] = gamma k^_j . k^_t and cq[t][j] = gamma k^_j . q^_t with
-            //      gamma = the decays strictly after j up to t; cq[t][t] = k^_t . q^_t;
-            //      Gamma_t = all its decays, kept as Gamma_t / |k_t| and Gamma_t / |q_t|.
-            //      The eight lanes of node t = tw + 4 (lane >> 3) walk its path in
-            //      step; lane l owns entries j0 = 2 (l & 7) and j0 + 1 and writes
-            //      them over KA, QA (KA's diagonal, which other nodes read for |k_j|,
-            //      is written back unchanged). ---------------------------------------
-            float rk_t = 0.f;
-            {
-                const int t = tw + 4 * (lane >> 3), j0 = 2 * (lane & 7);
-                float ck0 = 0.f, cq0 = 0.f, ck1 = 0.f, cq1 = 0.f;
-                if (t < lc) {
-                    const float rkt = rsqrtf(ka[t * (kSeg + 1)] + kb[t * (kSeg + 1)] + 1e-6f);
-                    const float rqt = rsqrtf(qqa[t] + qqb[t] + 1e-6f);
-                    if (j0 == t) ck0 = ka[t * (kSeg + 1)];
-                    if (j0 + 1 == t) ck1 = ka[t * (kSeg + 1)];
-                    float gam = 1.f;
-                    for (int cur = t;;) {
-                        gam *= dec_s[cur];
-                        cur = par[cur];
-                        if (cur < 0) break;
-                        if ((cur >> 1) == (j0 >> 1)) {
-                            const float rj = rsqrtf(ka[cur * (kSeg + 1)] + kb[cur * (kSeg + 1)] + 1e-6f);
-                            const float ck = gam * (ka[t * kSeg + cur] + kb[t * kSeg + cur]) * (rkt * rj);
-                            const float cq = gam * (qa[t * kSeg + cur] + qb[t * kSeg + cur]) * (rqt * rj);
-                            if (cur == j0) {
-                                ck0 = ck;
-                                cq0 = cq;
-                            } else {
-                                ck1 = ck;
-                                cq1 = cq;
-                            }
-                        }
-                    }
-                    const float self = (qa[t * (kSeg + 1)] + qb[t * (kSeg + 1)]) * (rqt * rkt);
-                    if (j0 == t) cq0 = self;
-                    if (j0 + 1 == t) cq1 = self;
-                    if ((lane & 7) == 0) {
-                        gsk[t] = gam * rkt;
-                        gsq[t] = gam * rqt;
-                    }
-                    rk_t = rkt;
-                }
-                __syncwarp();  // every lane of the warp has read its Gram terms
-                if (t < lc) {
-                    *reinterpret_cast<float2 *>(ka + t * kSeg + j0) = make_float2(ck0, ck1);
-                    *reinterpret_cast<float2 *>(qa + t * kSeg + j0) = make_float2(cq0, cq1);
+            // ---- C: path coefficients, two entries (t, j) per thread.
+            //      L[t][j] = beta_t gamma_{j->t} k^_j . k^_t (j a strict ancestor of t),
+            //      CQ[t][j] = q_scale gamma_{j->t} k^_j . q^_t (j on the path of t,
+            //      t included; stored transposed), column factors Gamma_t / |k_t|
+            //      and q_scale Gamma_t / |q_t|.  Zero outside the sequence's nodes. -
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int e = ttid + 128 * q2, t = e >> 4, j = e & (kSeg - 1);
+                const float rkt = rsqrtf(ka[t * (kSeg + 1)] + kb[t * (kSeg + 1)] + 1e-6f);
+                const float rkj = rsqrtf(ka[j * (kSeg + 1)] + kb[j * (kSeg + 1)] + 1e-6f);
+                const float rqt = rsqrtf(qqa[t] + qqb[t] + 1e-6f);
+                const float g = gm[e];
+                const bool in = t < lc;
+                const float lk = (in && j < t) ? beta_s[t] * (g * ((ka[e] + kb[e]) * (rkt * rkj))) : 0.f;
+                const float c = (in && j <= t) ? a.q_scale * (g * ((qa[e] + qb[e]) * (rqt * rkj))) : 0.f;
+                lnt[j * kSeg + t] = -lk;
+                cqt[j * kSeg + t] = c;
+                if (j == 0) {
+                    gsk[t] = gam_s[t] * rkt;
+                    gsq[t] = a.q_scale * (gam_s[t] * rqt);
+                    rk_s[t] = rkt;
                 }
             }
+            team_sync(team);  // coefficients of every node are in
+
+            // ---- D: the replay rows' k^ and this thread's v ----------------------
             // replay: k^ of this warp's nodes, from B's raw rows
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int t = tw + 4 * m;
-                const float r = __shfl_sync(0xffffffffu, rk_t, 8 * m);
                 if (t < lc && staged)
                     *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride + 4 * lane) =
-                        scale4(*reinterpret_cast<const float4 *>(bt_t + sw_off(t, 4 * lane, kBChunk)), r);
+                        scale4(*reinterpret_cast<const float4 *>(bt_t + sw_off(t, 4 * lane, kBChunk)), rk_s[t]);
             }
             // v of this thread's row, loaded while the accumulators finish
             float vreg[kSeg];
 #pragma unroll
-            for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? __ldg(a.xc + (n0 + t) * C + voff + row) : 0.0f;
-            team_sync(team);  // coefficients of every node are in
+            for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? gdn::ldg_pinned(a.xc + (n0 + t) * int64_t(a.C) + voff + row) : 0.f;
+            team_sync(team);  // B is no longer read
 
-            // ---- E: per row, the nodes in order ------------------------------------
+            // ---- E: per row, r = beta (v - Gamma S0 k^), u = T r, o = Gamma S0 q^ + W r
             // warp-uniform: tcgen05.ld is warp-collective
             const bool ready =
                 __all_sync(0xffffffffu, wait_or_abort(bars + B_ACCFULL + team, uint32_t(ut & 1), abort_flag));
@@ -958,55 +943,77 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             if (ready) {
                 gdn::tc_fence_after_sync();
                 const uint32_t trow = tmem + TEAM_COLS * team + (uint32_t(tw * 32) << 16);
-                // D = the sum of the partial accumulators, added in fp32: the
-                // 2^10 A_lo 2^-8 B_hi part first (scaled back, exactly), then
-                // A_hi B_hi and A_hi B_lo of both K-halves
+                // D = the sum of the partial accumulators, added in fp32, smallest
+                // first: A_lo B_lo, A_lo B_hi, A_hi B_lo of both K-halves, then
+                // A_hi B_hi of both K-halves
                 float dv[32], p1[32];
-                gdn::tmem_ld32(trow + LHCOL, dv);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dv[i] *= 1.0f / (kLoScale * kBScale);
+                gdn::tmem_ld32(trow + LHCOL + 32u, dv);
 #pragma unroll 1
-                for (int part = 0; part < 4; ++part) {
-                    gdn::tmem_ld32(trow + 32u * part, p1);
+                for (int part = 0; part < 5; ++part) {
+                    const uint32_t col = part == 0 ? LHCOL : part == 1 ? 32u : part == 2 ? 96u : part == 3 ? 0u : 64u;
+                    gdn::tmem_ld32(trow + col, p1);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) dv[i] += p1[i];
                 }
                 gdn::tc_fence_before_sync();
                 mbar_arrive(bars + B_ACCEMPTY + team);  // the accumulators may be overwritten
 
-                // S' k_t and o_t / q_scale each accumulate as a packed pair over
-                // even and odd j (ck, cq pairs times (u_2p, u_2p+1)), folded at
-                // the end.  up[p] holds (u_2p, u_2p+1), with zeros not yet known.
-                uint64_t up[kSeg / 2];
-                float uprev = 0.f;
+                // r_t = beta_t (v_t - Gamma_t S0 k^_t) and (I + L) u = r by forward
+                // substitution in column order: once column j - 1 is in, u_j is
+                // final and column j of -L times u_j goes into the later nodes.
+                // Nodes travel as packed pairs (u_2p, u_2p+1), so a column costs
+                // at most 8 paired FMAs and the chain from u_j to u_j+1 is one.
+                // Then o = Gamma S0 q^ + CQ u the same way.
+                uint64_t up[kSeg / 2], op[kSeg / 2];
+#pragma unroll
+                for (int p2 = 0; p2 < kSeg / 2; ++p2) {
+                    const int t = 2 * p2;
+                    const float r0 = beta_s[t] * (vreg[t] - gsk[t] * dv[t]);
+                    const float r1 = beta_s[t + 1] * (vreg[t + 1] - gsk[t + 1] * dv[t + 1]);
+                    up[p2] = gdn::f2pack(r0, r1);
+                    op[p2] = gdn::f2pack(gsq[t] * dv[kSeg + t], gsq[t + 1] * dv[kSeg + t + 1]);
+                }
+#pragma unroll
+                for (int j = 0; j < kSeg - 1; ++j) {
+                    const float2 u01 = gdn::f2unpack(up[j / 2]);
+                    const float uj = (j & 1) ? u01.y : u01.x;
+                    const uint64_t ujj = gdn::f2pack(uj, uj);
+                    const ulonglong2 *lcol = reinterpret_cast<const ulonglong2 *>(lnt + j * kSeg);
+#pragma unroll
+                    for (int q4 = j / 4; q4 < kSeg / 4; ++q4) {  // entries t = 4 q4 .. 4 q4 + 3 (zero for t <= j)
+                        const ulonglong2 c = lcol[q4];
+                        up[2 * q4] = gdn::fma2(c.x, ujj, up[2 * q4]);
+                        up[2 * q4 + 1] = gdn::fma2(c.y, ujj, up[2 * q4 + 1]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kSeg; ++j) {
+                    const float2 u01 = gdn::f2unpack(up[j / 2]);
+                    const float uj = (j & 1) ? u01.y : u01.x;
+                    const uint64_t ujj = gdn::f2pack(uj, uj);
+                    const ulonglong2 *ccol = reinterpret_cast<const ulonglong2 *>(cqt + j * kSeg);
+#pragma unroll
+                    for (int q4 = j / 4; q4 < kSeg / 4; ++q4) {  // entries t = 4 q4 .. 4 q4 + 3 (zero for t < j)
+                        const ulonglong2 c = ccol[q4];
+                        op[2 * q4] = gdn::fma2(c.x, ujj, op[2 * q4]);
+                        op[2 * q4 + 1] = gdn::fma2(c.y, ujj, op[2 * q4 + 1]);
+                    }
+                }
+                float *orow = a.o + (int64_t(n0) * a.Hv + h) * D + row;
+                float *urow = a.replay + (int64_t(n0) * a.Hv + h) * a.rstride + D + row;
+                const int64_t ostep = int64_t(a.Hv) * D, ustep = int64_t(a.Hv) * a.rstride;
 #pragma unroll
                 for (int t = 0; t < kSeg; ++t) {
-                    if (!(t & 1)) up[t / 2] = 0;
                     if (t < lc) {
-                        const int64_t n = n0 + t;
-                        uint64_t sk2 = gdn::f2pack(gsk[t] * dv[t], 0.f), oq2 = gdn::f2pack(gsq[t] * dv[kSeg + t], 0.f);
-#pragma unroll
-                        for (int j4 = 0; j4 < (t + 3) / 4; ++j4) {
-                            // pairs 2 j4 and 2 j4 + 1; a pair holding j = t sees u_t = 0
-                            const ulonglong2 ck = *reinterpret_cast<const ulonglong2 *>(ka + t * kSeg + 4 * j4);
-                            const ulonglong2 cq = *reinterpret_cast<const ulonglong2 *>(qa + t * kSeg + 4 * j4);
-                            sk2 = gdn::fma2(ck.x, up[2 * j4], sk2);
-                            oq2 = gdn::fma2(cq.x, up[2 * j4], oq2);
-                            if (4 * j4 + 2 < t) {
-                                sk2 = gdn::fma2(ck.y, up[2 * j4 + 1], sk2);
-                                oq2 = gdn::fma2(cq.y, up[2 * j4 + 1], oq2);
-                            }
-                        }
-                        const float2 sk = gdn::f2unpack(sk2), oq = gdn::f2unpack(oq2);
-                        const float ut = beta_s[t] * (vreg[t] - (sk.x + sk.y));
-                        up[t / 2] = (t & 1) ? gdn::f2pack(uprev, ut) : gdn::f2pack(ut, 0.f);
-                        uprev = ut;
-                        const float o = fmaf(qa[t * kSeg + t], ut, oq.x + oq.y);
-                        a.o[(n * a.Hv + h) * D + row] = a.q_scale * o;
-                        a.replay[(n * a.Hv + h) * a.rstride + D + row] = ut;
+                        const float2 o01 = gdn::f2unpack(op[t / 2]), u01 = gdn::f2unpack(up[t / 2]);
+                        orow[t * ostep] = (t & 1) ? o01.y : o01.x;
+                        urow[t * ustep] = (t & 1) ? u01.y : u01.x;
                     }
                 }
             }
+            // the lo rows of the next item's B (its q/k rows were requested when
+            // this item's accumulators completed and have landed meanwhile)
+            staged_nx = ready && split_b(v + 2);
             // after a timeout the team keeps looping (every wait now returns at
             // once) so that all four warps meet at each team barrier
         }
@@ -1071,25 +1078,28 @@ int sm_count() {
     return n;
 }
 
-// xc viewed as [N rows][C floats]; boxes of [16 rows][32 floats] (the q or k
-// rows of one sequence's 16 nodes, one K-chunk) in the 128-byte swizzle, so a
-// box lands as 16 rows of the tensor cores' K-major operand
-int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C) {
+// xc viewed as [N rows][C floats] with boxes of [rows][cols] floats.  The q/k
+// map takes boxes of [16 rows][32 floats] (the q or k rows of one sequence's
+// 16 nodes, one K-chunk) in the 128-byte swizzle, so a box lands as 16 rows of
+// the tensor cores' K-major operand; the v map takes [16 rows][d floats]
+// unswizzled (row t of the box = node t's v, contiguous).
+int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C, uint32_t rows, uint32_t cols,
+                  bool swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return GDN_ERR_TMA;
     cuuint64_t gdim[2] = {cuuint64_t(C), cuuint64_t(N)};
     cuuint64_t gstride[1] = {cuuint64_t(C) * 4};
-    cuuint32_t box[2] = {32, 16};
+    cuuint32_t box[2] = {cols, rows};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(xc), gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
 }
 
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     CUtensorMap xmap;
-    if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C)) return rc;
+    if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C, 16, 32, true)) return rc;
     auto k = tree_verify_ws_kernel;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(wsv::BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;

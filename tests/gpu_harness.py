@@ -160,15 +160,24 @@ def run_oracle(b: Batch, ssm: np.ndarray, conv_hist: np.ndarray, q_scale: float 
     return OracleOut(xc, win, o, rep, ssm2, hist2)
 
 
+def replay_parts(rep: np.ndarray, d: int):
+    """The three parts of replay rows [..., 2d + 1]: k^, u, decay."""
+    return {"replay_k": rep[..., :d], "replay_u": rep[..., d:2 * d], "replay_decay": rep[..., 2 * d]}
+
+
 def compare(g: GpuOut, r: OracleOut, tol: float = TOL, check_xc: bool = True):
-    """Element-by-element parity; returns the error figures."""
+    """Element-by-element parity; returns the error figures.  The replay rows
+    are judged part by part (k^, u, decay), each against its own scale."""
     assert g.status == 0, G.gdn_status_str(g.status)
     errs = {}
     if check_xc:
         errs["xc"] = relerr(g.xc, r.xc)
         assert np.array_equal(g.win, r.win), "commit windows differ"
     errs["o"] = relerr(g.o, r.o)
-    errs["replay"] = relerr(g.replay, r.replay)
+    d = g.o.shape[-1] if g.o.size else (g.replay.shape[-1] - 1) // 2
+    gp, rp = replay_parts(g.replay, d), replay_parts(r.replay, d)
+    for k in gp:
+        errs[k] = relerr(gp[k], rp[k])
     for k, v in errs.items():
         assert v <= tol, (k, v)
     return errs

@@ -60,46 +60,29 @@ def test_small_configs_all_rounds(cfg, rounds):
     print(cfg, {k: f"{v:.2e}" for k, v in worst.items()})
 
 
-def test_layer_stack_sampled_layers():
+def test_layer_stack_every_layer():
     """48-layer stack (5 sequences of {4,8,12,16,16} nodes, grouped 3:1):
-    round 0 of a sample of layers, each with its own weights and pools."""
+    round 0 of every layer, each with its own weights and pools, then three
+    carried rounds on the first and the last layer."""
     sp = W.spec(3)
-    for layer in (0, 13, 31, 47):
-        run_rounds(sp, [0], layer=layer)
+    worst = {}
+    for layer in range(sp.layers):
+        for k, v in run_rounds(sp, [0], layer=layer).items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    for layer in (0, sp.layers - 1):
+        for k, v in run_rounds(sp, range(3), layer=layer).items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    print("stack48", {k: f"{v:.2e}" for k, v in worst.items()})
 
 
 @pytest.mark.parametrize("variant", W.SWEEP_VARIANTS)
-def test_sweep_full_size_sampled(variant):
-    """The benchmark's workload at full size (64 sequences, 128-slot pool), in
-    the benchmark's launch configuration; the oracle checks a sample of
-    sequences one by one (sequences are independent)."""
+def test_sweep_full_size_three_rounds(variant):
+    """The benchmark's workload at full size (64 sequences, 128-slot pool) in
+    the benchmark's launch configuration: rounds 0-2 with the pools carried,
+    every sequence compared with the oracle."""
     sp = W.sweep_spec(variant)
-    lp = W.layer_params(sp)
-    sm = W.slot_map(sp)
-    ri = W.round_inputs(sp, 0, 0)
-    b = batch_from(sp, lp, ri, sm, max_nodes=sp.max_seq_nodes)
-    pools = GpuPools(lp.ssm, lp.conv_hist)
-    g = run_gpu(b, pools)
-    assert g.status == 0
-    ssm_gpu = pools.ssm.cpu().numpy()
-    hist_gpu = pools.conv_hist.cpu().numpy()
-    committed = {int(sm[s]) for s in range(b.S) if b.accepted[s] >= 0}
-    untouched = sorted(set(range(b.P)) - committed)
-    assert np.array_equal(ssm_gpu[untouched], lp.ssm[untouched])
-    assert np.array_equal(hist_gpu[untouched], lp.conv_hist[untouched])
-    for s in (0, 37, 63):
-        sub = W.subset(sp, ri, [s])
-        bs = batch_from(sp, lp, sub, sm[[s]], max_nodes=sp.max_seq_nodes)
-        ref = run_oracle(bs, lp.ssm, lp.conv_hist)
-        n0, n1 = int(ri.node_off[s]), int(ri.node_off[s + 1])
-        assert relerr(g.xc[n0:n1], ref.xc) <= TOL
-        assert np.array_equal(g.win[n0:n1], ref.win)
-        assert relerr(g.o[n0:n1], ref.o) <= TOL
-        assert relerr(g.replay[n0:n1], ref.replay) <= TOL
-        slot = int(sm[s])
-        if b.accepted[s] >= 0:
-            assert relerr(ssm_gpu[slot], ref.ssm[slot]) <= TOL
-        assert np.array_equal(hist_gpu[slot], ref.conv_hist[slot])
+    worst = run_rounds(sp, range(3), max_nodes=sp.max_seq_nodes)
+    print(variant, {k: f"{v:.2e}" for k, v in worst.items()})
 
 
 # ---------------------------------------------------------------- edge cases
