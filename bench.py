@@ -83,13 +83,16 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------ algorithmic bytes
-def algo_bytes(sp: W.Spec, parents: np.ndarray, node_off: np.ndarray, accepted: np.ndarray):
-    """Bytes the method must move per launch (conv weights once per layer)."""
+def algo_bytes(sp: W.Spec, parents: np.ndarray, node_off: np.ndarray, accepted: np.ndarray,
+               compact: bool = False):
+    """Bytes the method must move per launch (conv weights once per layer).
+    compact: windows travel as three int32 references per node, and the commit
+    gathers the accepted window (3 C floats) from x and the history."""
     sh = sp.shape
     S, Hv, d = sh.n_seqs, sh.h_v, sh.d
     C = sh.conv_channels
     N = int(node_off[-1])
-    conv = N * C * 4 + S * 3 * C * 4 + 16 * C + N * C * 4 + N * 3 * C * 4
+    conv = N * C * 4 + S * 3 * C * 4 + 16 * C + N * C * 4 + (N * 3 * 4 if compact else N * 3 * C * 4)
     verify = S * Hv * d * d * 4 + N * C * 4 + N * 2 * Hv * 4 + N * Hv * d * 4 + N * Hv * (2 * d + 1) * 4
     commit = 0
     for s in range(S):
@@ -101,7 +104,7 @@ def algo_bytes(sp: W.Spec, parents: np.ndarray, node_off: np.ndarray, accepted: 
         while a >= 0:
             m += 1
             a = int(parents[n0 + a])
-        commit += 2 * Hv * d * d * 4 + m * Hv * (2 * d + 1) * 4 + 2 * 3 * C * 4
+        commit += 2 * Hv * d * d * 4 + m * Hv * (2 * d + 1) * 4 + 2 * 3 * C * 4 + (3 * 4 if compact else 0)
     return {"conv": conv, "verify": verify, "commit": commit}
 
 
@@ -171,7 +174,8 @@ class DeviceWorkload:
     the two pools) are drawn on the device with torch's Philox generator keyed
     by the same stream keys, with the same distributions."""
 
-    def __init__(self, sp: W.Spec, rounds: int, device, seed_offset: int = 0, layer: int = 0):
+    def __init__(self, sp: W.Spec, rounds: int, device, seed_offset: int = 0, layer: int = 0,
+                 compact: bool = False):
         import torch
         self.sp, self.device = sp, device
         sh = sp.shape
@@ -198,7 +202,9 @@ class DeviceWorkload:
         N = int(self.host_rounds[0].node_off[-1])
         self.N = N
         self.xc = torch.empty((N, self.C), device=device)
-        self.win = torch.empty((N, 3, self.C), device=device)
+        self.compact = compact
+        self.win = torch.empty((1 if compact else N, 3, self.C), device=device)
+        self.wref = torch.empty((N, 3), dtype=torch.int32, device=device)
         self.o = torch.empty((N, sh.h_v, sh.d), device=device)
         self.replay = torch.empty((N, sh.h_v, self.rs), device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -212,8 +218,12 @@ class DeviceWorkload:
         R = inputs if inputs is not None else self.rounds[r]
         if events:
             events[0].record()
-        G.gdn_conv_tree_step(self.dims, R["x"], self.C, self.w, self.hist, R["parents"], R["node_off"],
-                             self.slot_map, self.xc, self.win, self.status)
+        if self.compact:
+            G.gdn_conv_tree_step_compact(self.dims, R["x"], self.C, self.w, self.hist, R["parents"],
+                                         R["node_off"], self.slot_map, self.xc, self.wref, self.status)
+        else:
+            G.gdn_conv_tree_step(self.dims, R["x"], self.C, self.w, self.hist, R["parents"], R["node_off"],
+                                 self.slot_map, self.xc, self.win, self.status)
         if events:
             events[1].record()
         G.gdn_tree_verify(self.dims, self.xc, R["ba"], 2 * sh.h_v, self.dt, self.A, self.ssm, 1.0,
@@ -221,8 +231,12 @@ class DeviceWorkload:
                           self.status)
         if events:
             events[2].record()
-        G.gdn_commit(self.dims, R["accepted"], R["parents"], R["node_off"], self.slot_map, self.replay,
-                     self.rs, self.win, self.ssm, self.hist, self.status)
+        if self.compact:
+            G.gdn_commit_compact(self.dims, R["accepted"], R["parents"], R["node_off"], self.slot_map,
+                                 self.replay, self.rs, R["x"], self.C, self.wref, self.ssm, self.hist, self.status)
+        else:
+            G.gdn_commit(self.dims, R["accepted"], R["parents"], R["node_off"], self.slot_map, self.replay,
+                         self.rs, self.win, self.ssm, self.hist, self.status)
         if events:
             events[3].record()
 
@@ -254,8 +268,9 @@ def ncu_traffic(kernel: str, variant: str):
 def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int = 0,
                  e2e: bool = False, clocks: bool = False):
     import torch
-    sp = W.sweep_spec(variant, rounds=N_ROUNDS)
-    wl = DeviceWorkload(sp, min(N_ROUNDS, max(steps + warmup, 1)), device, seed_offset)
+    compact = variant.endswith("_compact")
+    sp = W.sweep_spec(variant[: -len("_compact")] if compact else variant, rounds=N_ROUNDS)
+    wl = DeviceWorkload(sp, min(N_ROUNDS, max(steps + warmup, 1)), device, seed_offset, compact=compact)
     flush = L2Flush(device)
     nr = len(wl.rounds)
     for i in range(warmup):
@@ -299,7 +314,7 @@ def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int
         per["commit"].append(e[2].elapsed_time(e[3]))
         step_ms_kernel_events.append(e[0].elapsed_time(e[3]))
     bytes_ = [algo_bytes(sp, wl.host_rounds[(warmup + i) % nr].parents, wl.host_rounds[(warmup + i) % nr].node_off,
-                         wl.host_rounds[(warmup + i) % nr].accepted) for i in range(steps)]
+                         wl.host_rounds[(warmup + i) % nr].accepted, compact) for i in range(steps)]
     out = {"sp": sp, "wl": wl, "step_ms": step_ms, "step_ms_kernel_events": step_ms_kernel_events, "per": per,
            "bytes": bytes_,
            "clocks": sampler.summary() if sampler else None}
@@ -509,6 +524,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variants", default="all", help="'all' or a comma list of sweep variants")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default="1,2,3",
+                    help="smaller workloads timed as whole steps (comma list of 1, 2, 3; 'none')")
     ap.add_argument("--l2-dirty", action="store_true", help="flush L2 by the write alone (no draining read)")
     args = ap.parse_args()
     global L2_DIRTY
@@ -533,11 +550,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
 
-    variants = list(W.SWEEP_VARIANTS) if args.variants == "all" else args.variants.split(",")
+    variants = (list(W.SWEEP_VARIANTS) + [HEADLINE + "_compact"] if args.variants == "all"
+                else args.variants.split(","))
     if HEADLINE in variants:
         variants.remove(HEADLINE)
     head = time_variant(HEADLINE, args.steps, args.warmup, device, seed_offset=rank, e2e=True, clocks=True)
     others = {v: time_variant(v, args.steps, args.warmup, device, seed_offset=rank) for v in variants}
+    cfg_ids = [] if args.configs in ("", "none") else [int(c) for c in args.configs.split(",")]
+    configs = {W.SPEC_NAMES[c]: time_config(c, min(args.steps, 20), args.warmup, device) for c in cfg_ids}
 
     sp = head["sp"]
     N = head["wl"].N
@@ -561,7 +581,9 @@ def main():
     dom = max(kern_ms, key=kern_ms.get)
     achieved = kb[dom] / (kern_ms[dom] * 1e-3) / 1e9
     traffic = ncu_traffic(dom, HEADLINE)
-    kernels = {k: {"ms": round(kern_ms[k], 5), "algo_bytes": int(kb[k]),
+    traffic_all = {k: ncu_traffic(k, HEADLINE) for k in kern_ms}
+    measured = sum(traffic_all.values()) if all(traffic_all.values()) else None
+    kernels = {k: {"ms": round(kern_ms[k], 5), "algo_bytes": int(kb[k]), "dram_bytes_ncu": traffic_all[k],
                    "gbs": round(kb[k] / (kern_ms[k] * 1e-3) / 1e9, 1),
                    "frac": round(kb[k] / (kern_ms[k] * 1e-3) / 1e9 / peak, 4),
                    "share": round(kern_ms[k] / sum(kern_ms.values()), 4)} for k in kern_ms}
@@ -575,11 +597,17 @@ def main():
                     "kernels_ms": {k: round(statistics.mean(x), 5) for k, x in r["per"].items()}}
 
     cpu = None
+    spot = None
     if not args.no_cpu_baseline:
-        nodes, secs, nseq = oracle_sample(HEADLINE)
-        cpu = {"value": round(nodes / secs, 2), "unit": "nodes/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nseq} of 64 sequences ({nodes} nodes) of the {HEADLINE} workload, "
-                         f"conv+verify+commit, {secs:.1f} s single-threaded C"}
+        spot = parity_spot(head["wl"])
+        nodes1, secs1, nseq1 = oracle_sample(HEADLINE)
+        nodes_n, secs_n, nseq_n, ncores = oracle_all_cores(HEADLINE)
+        cpu = {"value": round(nodes_n / secs_n, 2), "unit": "nodes/s", "cores": ncores, "kind": "oracle",
+               "sample": f"{nseq_n} whole sequences ({nodes_n} nodes) of the {HEADLINE} workload, "
+                         f"conv+verify+commit, one single-threaded oracle process per core for "
+                         f"{secs_n:.1f} s",
+               "single_core": {"value": round(nodes1 / secs1, 2), "unit": "nodes/s", "cores": 1,
+                               "sample": f"{nseq1} sequences ({nodes1} nodes), {secs1:.1f} s"}}
 
     line = {
         "metric": METRIC,
@@ -600,9 +628,14 @@ def main():
                    "parallelism": f"replicas x{world}",
                    "l2": L2Flush.describe_static()},
         "hbm": {"step_algo_bytes": int(step_bytes),
-                "step_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
-                "frac_of_peak": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+                "step_algo_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
+                "algo_frac_of_peak": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+                "step_dram_bytes_ncu": measured,
+                "step_dram_gbs_ncu": (round(measured / (step_ms * 1e-3) / 1e9, 1) if measured else None),
                 "peak_gbs": peak, "peak_kind": peak_kind,
+                "note": "algorithmic bytes = what the method must move; the ncu figure is the DRAM traffic "
+                        "of the same three kernels captured one launch each (null when a kernel changed "
+                        "since its capture)",
                 "ms_per_step_with_kernel_events": round(statistics.mean(head["step_ms_kernel_events"]), 5)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -614,8 +647,12 @@ def main():
                 "h2d_bytes_per_step": head["e2e"]["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": head["e2e"]["d2h_bytes_per_step"]},
         "gpu_launches": 4 * args.steps * (1 + len(others)),
+        "gpu_launches_note": "timed head steps x 4 launches (conv, verify, commit preflight, commit apply); "
+                             "the second whole-step pass and the sweep variants launch the same per step",
         "clocks": head["clocks"],
         "cpu_baseline": cpu,
+        "parity_spot": spot,
+        "configs": configs,
     }
     print(json.dumps(line))
     if dist is not None:

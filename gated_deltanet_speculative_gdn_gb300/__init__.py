@@ -28,8 +28,10 @@ GDN_ERR_NULL, GDN_ERR_DIMS, GDN_ERR_STRIDE, GDN_ERR_ALIGN = -1, -2, -3, -4
 GDN_ERR_ALIAS, GDN_ERR_LAUNCH, GDN_ERR_TMA = -5, -6, -7
 GDN_DEV_BAD_NODE_OFF, GDN_DEV_BAD_PARENT, GDN_DEV_BAD_SLOT = 1, 2, 3
 GDN_DEV_DUP_SLOT, GDN_DEV_BAD_ACCEPTED, GDN_DEV_TIMEOUT = 4, 5, 6
+GDN_DEV_BAD_WINDOW = 7
 
 EXPORTED_SYMBOLS = ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit",
+                    "gdn_conv_tree_step_compact", "gdn_commit_compact",
                     "gdn_status_str", "gdn_replay_row_floats")
 
 if not os.path.exists(LIB_PATH):
@@ -67,7 +69,10 @@ lib.gdn_conv_tree_step.argtypes = [_DP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P
 lib.gdn_tree_verify.argtypes = [_DP, _P, _P, _I64, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                                 _P, _P, _I64, _P, _P]
 lib.gdn_commit.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P]
-for _f in ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit"):
+lib.gdn_conv_tree_step_compact.argtypes = [_DP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+lib.gdn_commit_compact.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _P]
+for _f in ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit", "gdn_conv_tree_step_compact",
+           "gdn_commit_compact"):
     getattr(lib, _f).restype = ctypes.c_int
 lib.gdn_status_str.argtypes = [ctypes.c_int]
 lib.gdn_status_str.restype = ctypes.c_char_p
@@ -135,3 +140,20 @@ def gdn_commit(dims: GdnDims, accepted, parents, node_off, slot_map, replay, rep
                         _ptr(slot_map), _ptr(replay), int(replay_stride), _ptr(win), _ptr(ssm),
                         _ptr(conv_hist), _ptr(status), _stream(stream))
     return _check("gdn_commit", rc, raise_on_error)
+
+
+def gdn_conv_tree_step_compact(dims: GdnDims, x, x_stride: int, conv_w, conv_hist, parents, node_off,
+                               slot_map, xc, win_ref, status, stream=None, raise_on_error: bool = True) -> int:
+    rc = lib.gdn_conv_tree_step_compact(ctypes.byref(dims), _ptr(x), int(x_stride), _ptr(conv_w),
+                                        _ptr(conv_hist), _ptr(parents), _ptr(node_off), _ptr(slot_map),
+                                        _ptr(xc), _ptr(win_ref), _ptr(status), _stream(stream))
+    return _check("gdn_conv_tree_step_compact", rc, raise_on_error)
+
+
+def gdn_commit_compact(dims: GdnDims, accepted, parents, node_off, slot_map, replay, replay_stride: int,
+                       x, x_stride: int, win_ref, ssm, conv_hist, status, stream=None,
+                       raise_on_error: bool = True) -> int:
+    rc = lib.gdn_commit_compact(ctypes.byref(dims), _ptr(accepted), _ptr(parents), _ptr(node_off),
+                                _ptr(slot_map), _ptr(replay), int(replay_stride), _ptr(x), int(x_stride),
+                                _ptr(win_ref), _ptr(ssm), _ptr(conv_hist), _ptr(status), _stream(stream))
+    return _check("gdn_commit_compact", rc, raise_on_error)

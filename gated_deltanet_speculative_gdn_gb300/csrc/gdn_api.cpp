@@ -18,6 +18,7 @@ extern "C" const char *gdn_status_str(int code) {
         case GDN_DEV_DUP_SLOT: return "GDN_DEV_DUP_SLOT";
         case GDN_DEV_BAD_ACCEPTED: return "GDN_DEV_BAD_ACCEPTED";
         case GDN_DEV_TIMEOUT: return "GDN_DEV_TIMEOUT";
+        case GDN_DEV_BAD_WINDOW: return "GDN_DEV_BAD_WINDOW";
         default: return "unknown";
     }
 }

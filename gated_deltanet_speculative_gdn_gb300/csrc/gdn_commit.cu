@@ -36,7 +36,10 @@ struct CommitArgs {
     const int32_t *__restrict__ slot_map;
     const float *__restrict__ replay;
     int64_t rstride;
-    const float *__restrict__ win;
+    const float *__restrict__ win;      // [N][3][C] windows, or (compact form)
+    const int32_t *__restrict__ wref;   // [N][3] window references into x / the history
+    const float *__restrict__ x;        // [N][x_stride] tokens (compact form only)
+    int64_t x_stride;
     float *ssm;
     float *hist;
     int32_t *status;
@@ -73,6 +76,12 @@ __global__ void __launch_bounds__(256) commit_preflight_kernel(const CommitArgs 
             for (int s2 = lane; s2 < a.S; s2 += 32)
                 dup |= (s2 != s && a.accepted[s2] >= 0 && a.slot_map[s2] == slot);
             if (!err && __any_sync(0xffffffffu, dup)) err = GDN_DEV_DUP_SLOT;
+            if (!err && a.wref) {
+                for (int j = 0; j < 3; ++j) {
+                    const int r = a.wref[(int64_t(n0) + acc) * 3 + j];
+                    if (r < -3 || r >= a.N) err = GDN_DEV_BAD_WINDOW;
+                }
+            }
         }
     }
     if (err && lane == 0) gdn::record_status(a.status, err);
@@ -179,7 +188,7 @@ __global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const
             gam_s = gam;
             m_s = m;
         }
-    } else {
+    } else if (!a.wref) {
         // warps 1-3: their share of the window copy, conv_hist[slot] <- win[accepted]
         const int64_t total4 = int64_t(3) * a.C / 4;
         const int64_t parts = int64_t(a.Hv) * CPH * (kApplyWarps - 1);
@@ -188,6 +197,29 @@ __global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const
         const float4 *wsrc = reinterpret_cast<const float4 *>(a.win + (int64_t(n0) + acc) * 3 * a.C);
         float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(slot) * 3 * a.C);
         for (int64_t i = lo + lane; i < hi; i += 32) hdst[i] = __ldg(wsrc + i);
+    } else {
+        // warps 1-3, compact form: their share of the channel groups of the new
+        // history, gathered through the accepted node's references from x rows
+        // and the slot's old history; a thread reads all three columns of its
+        // channel group before writing any, so in-place reuse of an old column
+        // is safe (and no other thread touches that channel group)
+        const int64_t total4 = a.C / 4;
+        const int64_t parts = int64_t(a.Hv) * CPH * (kApplyWarps - 1);
+        const int64_t per = (total4 + parts - 1) / parts;
+        const int64_t lo = ((int64_t(h) * CPH + q) * (kApplyWarps - 1) + warp - 1) * per, hi = min(total4, lo + per);
+        const int32_t *ref = a.wref + (int64_t(n0) + acc) * 3;
+        const int r0 = ref[0], r1 = ref[1], r2 = ref[2];
+        float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(slot) * 3 * a.C);
+        auto col = [&](int r, int64_t i) -> float4 {
+            return r >= 0 ? __ldg(reinterpret_cast<const float4 *>(a.x + int64_t(r) * a.x_stride) + i)
+                          : hdst[(-1 - r) * (a.C / 4) + i];
+        };
+        for (int64_t i = lo + lane; i < hi; i += 32) {
+            const float4 v0 = col(r0, i), v1 = col(r1, i), v2 = col(r2, i);
+            hdst[i] = v0;
+            hdst[a.C / 4 + i] = v1;
+            hdst[2 * (a.C / 4) + i] = v2;
+        }
     }
     __syncthreads();
     const int m = m_s;
@@ -235,23 +267,23 @@ __global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const
     }
 }
 
-}  // namespace
-
-extern "C" int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const int32_t *parents,
-                          const int32_t *node_off, const int32_t *slot_map, const float *replay,
-                          int64_t replay_stride, const float *win, float *ssm, float *conv_hist,
-                          int32_t *status, void *stream) {
+int commit_entry(const gdn_dims *dims, const int32_t *accepted, const int32_t *parents, const int32_t *node_off,
+                 const int32_t *slot_map, const float *replay, int64_t replay_stride, const float *win,
+                 const float *x, int64_t x_stride, const int32_t *wref, float *ssm, float *conv_hist,
+                 int32_t *status, void *stream) {
     int rc = gdn::check_dims(dims);
     if (rc) return rc;
     const int64_t S = dims->n_seqs, N = dims->n_nodes, P = dims->n_slots;
     const int64_t Hv = dims->h_v, D = dims->d_k, C = gdn::conv_channels(dims);
+    const bool compact = wref != nullptr;
     if (!status) return GDN_ERR_NULL;
     if (S == 0) return GDN_OK;
     if (!accepted || !node_off || !slot_map || !ssm || !conv_hist) return GDN_ERR_NULL;
-    if (N > 0 && (!parents || !replay || !win)) return GDN_ERR_NULL;
+    if (N > 0 && (!parents || !replay || (compact ? !x : !win))) return GDN_ERR_NULL;
     if (replay_stride < 2 * D + 1 || replay_stride % 4 != 0) return GDN_ERR_STRIDE;
-    if (!gdn::aligned16(ssm) || !gdn::aligned16(conv_hist) || (N > 0 && (!gdn::aligned16(replay) ||
-                                                                         !gdn::aligned16(win))))
+    if (compact && (x_stride < C || x_stride % 4 != 0)) return GDN_ERR_STRIDE;
+    if (!gdn::aligned16(ssm) || !gdn::aligned16(conv_hist) ||
+        (N > 0 && (!gdn::aligned16(replay) || (compact ? !gdn::aligned16(x) : !gdn::aligned16(win)))))
         return GDN_ERR_ALIGN;
     const gdn::Span outs[] = {{ssm, size_t(P * Hv * D * D * 4)}, {conv_hist, size_t(P * 3 * C * 4)}};
     const gdn::Span ins[] = {{accepted, size_t(S * 4)},
@@ -259,12 +291,13 @@ extern "C" int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const i
                              {node_off, size_t((S + 1) * 4)},
                              {slot_map, size_t(S * 4)},
                              {replay, gdn::strided_bytes(N * Hv, replay_stride, 2 * D + 1)},
-                             {win, size_t(N * 3 * C * 4)},
+                             compact ? gdn::Span{x, gdn::strided_bytes(N, x_stride, C)} : gdn::Span{win, size_t(N * 3 * C * 4)},
+                             {wref, compact ? size_t(N * 3 * 4) : 0},
                              {status, 4}};
-    if ((rc = gdn::check_alias(outs, 2, ins, 7))) return rc;
+    if ((rc = gdn::check_alias(outs, 2, ins, 8))) return rc;
 
-    CommitArgs a{accepted, parents, node_off, slot_map, replay, replay_stride, win, ssm, conv_hist, status,
-                 int(S), int(N), int(P), int(Hv), int(C), dims->max_seq_nodes};
+    CommitArgs a{accepted, parents, node_off, slot_map, replay, replay_stride, compact ? nullptr : win, wref, x,
+                 x_stride, ssm, conv_hist, status, int(S), int(N), int(P), int(Hv), int(C), dims->max_seq_nodes};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (gdn::launch_pdl(commit_preflight_kernel, dim3(unsigned((S + 7) / 8)), dim3(256), 0, st, a) != cudaSuccess)
         return GDN_ERR_LAUNCH;
@@ -280,4 +313,25 @@ extern "C" int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const i
         default: e = gdn::launch_pdl(commit_apply_kernel<128>, grid, block, 0, st, a); break;
     }
     return e == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const int32_t *parents,
+                          const int32_t *node_off, const int32_t *slot_map, const float *replay,
+                          int64_t replay_stride, const float *win, float *ssm, float *conv_hist,
+                          int32_t *status, void *stream) {
+    if (dims && dims->n_nodes > 0 && !win) return GDN_ERR_NULL;
+    return commit_entry(dims, accepted, parents, node_off, slot_map, replay, replay_stride, win, nullptr, 0, nullptr,
+                        ssm, conv_hist, status, stream);
+}
+
+extern "C" int gdn_commit_compact(const gdn_dims *dims, const int32_t *accepted, const int32_t *parents,
+                                  const int32_t *node_off, const int32_t *slot_map, const float *replay,
+                                  int64_t replay_stride, const float *x, int64_t x_stride,
+                                  const int32_t *win_ref, float *ssm, float *conv_hist, int32_t *status,
+                                  void *stream) {
+    if (dims && dims->n_nodes > 0 && !win_ref) return GDN_ERR_NULL;
+    return commit_entry(dims, accepted, parents, node_off, slot_map, replay, replay_stride, nullptr, x, x_stride,
+                        win_ref, ssm, conv_hist, status, stream);
 }

@@ -33,7 +33,8 @@ struct ConvArgs {
     const int32_t *__restrict__ node_off;
     const int32_t *__restrict__ slot_map;
     float *__restrict__ xc;
-    float *__restrict__ win;
+    float *__restrict__ win;      // [N][3][C] windows (copies), or
+    int32_t *__restrict__ wref;   // [N][3] window references (compact form)
     int32_t *status;
     int S, N, P, C, max_nodes;
 };
@@ -42,6 +43,10 @@ __device__ __forceinline__ float4 silu4(float4 v) {
     return make_float4(gdn::silu_f(v.x), gdn::silu_f(v.y), gdn::silu_f(v.z), gdn::silu_f(v.w));
 }
 
+// kCompact: instead of the window rows, each node's window is written as three
+// references (oldest first): a global node index (an x row) or -1 - k for
+// history column k of the slot; the commit gathers from x and the history.
+template <bool kCompact>
 __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const ConvArgs a) {
     const int s = blockIdx.y;
     const int tid = threadIdx.x;
@@ -98,6 +103,16 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
         }
     }
     __syncthreads();
+    if constexpr (kCompact) {
+        if (blockIdx.x == 0) {
+            for (int i = tid; i < ns; i += kConvThreads) {
+                int32_t *r = a.wref + (static_cast<int64_t>(n0) + i) * 3;
+                r[0] = src[i][1];
+                r[1] = src[i][0];
+                r[2] = n0 + i;
+            }
+        }
+    }
 
     const int lane = tid & 31, warp = tid >> 5;
     const int c4 = blockIdx.x * (kConvChannels / 4) + lane;  // float4 channel group
@@ -130,34 +145,34 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_step_kernel(const Conv
         acc.z = fmaf(c0.z, wc2.w, fmaf(c1.z, wc2.z, fmaf(c2.z, wc2.y, fmaf(c3.z, wc2.x, 0.0f))));
         acc.w = fmaf(c0.w, wc3.w, fmaf(c1.w, wc3.z, fmaf(c2.w, wc3.y, fmaf(c3.w, wc3.x, 0.0f))));
         *reinterpret_cast<float4 *>(a.xc + n * C + 4 * c4) = silu4(acc);
-        float *wrow = a.win + n * 3 * C + 4 * c4;
-        // the windows are read back only for the accepted node: stream them past L2
-        __stcs(reinterpret_cast<float4 *>(wrow), c2);
-        __stcs(reinterpret_cast<float4 *>(wrow + C), c1);
-        __stcs(reinterpret_cast<float4 *>(wrow + 2 * C), c0);
+        if constexpr (!kCompact) {
+            float *wrow = a.win + n * 3 * C + 4 * c4;
+            // the windows are read back only for the accepted node: stream them past L2
+            __stcs(reinterpret_cast<float4 *>(wrow), c2);
+            __stcs(reinterpret_cast<float4 *>(wrow + C), c1);
+            __stcs(reinterpret_cast<float4 *>(wrow + 2 * C), c0);
+        }
     }
 }
 
-}  // namespace
-
-extern "C" int gdn_conv_tree_step(const gdn_dims *dims, const float *x, int64_t x_stride,
-                                  const float *conv_w, const float *conv_hist,
-                                  const int32_t *parents, const int32_t *node_off,
-                                  const int32_t *slot_map, float *xc, float *win, int32_t *status,
-                                  void *stream) {
+int conv_entry(const gdn_dims *dims, const float *x, int64_t x_stride, const float *conv_w, const float *conv_hist,
+               const int32_t *parents, const int32_t *node_off, const int32_t *slot_map, float *xc, float *win,
+               int32_t *wref, int32_t *status, void *stream) {
     int rc = gdn::check_dims(dims);
     if (rc) return rc;
     const int64_t S = dims->n_seqs, N = dims->n_nodes, P = dims->n_slots;
     const int64_t C = gdn::conv_channels(dims);
+    const bool compact = wref != nullptr;
     if (!status) return GDN_ERR_NULL;
     if (S == 0 || N == 0) return GDN_OK;
-    if (!x || !conv_w || !conv_hist || !parents || !node_off || !slot_map || !xc || !win)
+    if (!x || !conv_w || !conv_hist || !parents || !node_off || !slot_map || !xc || (!win && !compact))
         return GDN_ERR_NULL;
     if (x_stride < C || x_stride % 4 != 0) return GDN_ERR_STRIDE;
-    if (!gdn::aligned16(x) || !gdn::aligned16(conv_w) || !gdn::aligned16(conv_hist) ||
-        !gdn::aligned16(xc) || !gdn::aligned16(win))
+    if (!gdn::aligned16(x) || !gdn::aligned16(conv_w) || !gdn::aligned16(conv_hist) || !gdn::aligned16(xc) ||
+        (!compact && !gdn::aligned16(win)))
         return GDN_ERR_ALIGN;
-    const gdn::Span outs[] = {{xc, size_t(N * C * 4)}, {win, size_t(N * 3 * C * 4)}};
+    const gdn::Span outs[] = {{xc, size_t(N * C * 4)},
+                              compact ? gdn::Span{wref, size_t(N * 3 * 4)} : gdn::Span{win, size_t(N * 3 * C * 4)}};
     const gdn::Span ins[] = {{x, gdn::strided_bytes(N, x_stride, C)},
                              {conv_w, size_t(C * 16)},
                              {conv_hist, size_t(P * 3 * C * 4)},
@@ -167,12 +182,34 @@ extern "C" int gdn_conv_tree_step(const gdn_dims *dims, const float *x, int64_t 
                              {status, 4}};
     if ((rc = gdn::check_alias(outs, 2, ins, 7))) return rc;
 
-    ConvArgs a{x, x_stride, conv_w, conv_hist, parents, node_off, slot_map, xc, win, status,
+    ConvArgs a{x, x_stride, conv_w, conv_hist, parents, node_off, slot_map, xc, win, wref, status,
                int(S), int(N), int(P), int(C), dims->max_seq_nodes};
     const int c4 = int(C / 4);
     const dim3 grid{unsigned((c4 + kConvChannels / 4 - 1) / (kConvChannels / 4)), unsigned(S)};
-    return gdn::launch_pdl(conv_tree_step_kernel, grid, dim3(kConvThreads), 0, static_cast<cudaStream_t>(stream),
-                           a) == cudaSuccess
+    auto k = compact ? conv_tree_step_kernel<true> : conv_tree_step_kernel<false>;
+    return gdn::launch_pdl(k, grid, dim3(kConvThreads), 0, static_cast<cudaStream_t>(stream), a) == cudaSuccess
                ? GDN_OK
                : GDN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" int gdn_conv_tree_step(const gdn_dims *dims, const float *x, int64_t x_stride,
+                                  const float *conv_w, const float *conv_hist,
+                                  const int32_t *parents, const int32_t *node_off,
+                                  const int32_t *slot_map, float *xc, float *win, int32_t *status,
+                                  void *stream) {
+    if (!win) return GDN_ERR_NULL;
+    return conv_entry(dims, x, x_stride, conv_w, conv_hist, parents, node_off, slot_map, xc, win, nullptr, status,
+                      stream);
+}
+
+extern "C" int gdn_conv_tree_step_compact(const gdn_dims *dims, const float *x, int64_t x_stride,
+                                          const float *conv_w, const float *conv_hist,
+                                          const int32_t *parents, const int32_t *node_off,
+                                          const int32_t *slot_map, float *xc, int32_t *win_ref,
+                                          int32_t *status, void *stream) {
+    if (!win_ref) return GDN_ERR_NULL;
+    return conv_entry(dims, x, x_stride, conv_w, conv_hist, parents, node_off, slot_map, xc, nullptr, win_ref,
+                      status, stream);
 }

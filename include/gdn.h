@@ -108,7 +108,8 @@ enum {
     GDN_DEV_BAD_SLOT = 3,      /* slot_map[s] outside [0, P)                      */
     GDN_DEV_DUP_SLOT = 4,      /* two committing sequences share a slot           */
     GDN_DEV_BAD_ACCEPTED = 5,  /* accepted[s] outside [-1, N_s)                   */
-    GDN_DEV_TIMEOUT = 6        /* a bounded wait in a kernel ran out              */
+    GDN_DEV_TIMEOUT = 6,       /* a bounded wait in a kernel ran out              */
+    GDN_DEV_BAD_WINDOW = 7     /* a window reference outside [-3, N) (compact)    */
 };
 
 /* Conv tree step (lucebox PR #707, Optimizations: fused convolution
@@ -179,6 +180,34 @@ int gdn_commit(const gdn_dims *dims, const int32_t *accepted, const int32_t *par
                const int32_t *node_off, const int32_t *slot_map, const float *replay,
                int64_t replay_stride, const float *win, float *ssm, float *conv_hist,
                int32_t *status, void *stream);
+
+/* Compact commit windows (lucebox PR #707, Optimizations: the conv tree step
+ * also produces the commit window; a window is three columns of the node's
+ * column sequence, so it can be named instead of copied).
+ * gdn_conv_tree_step_compact computes xc exactly as gdn_conv_tree_step but,
+ * instead of the window rows, writes for every node t
+ *     win_ref[t][j], j = 0..2 (oldest first)
+ * naming column j of t's commit window: a global node index n >= 0 (the
+ * window column is x row n) or -1 - k for column h_k of the slot's history.
+ * gdn_commit_compact then performs gdn_commit with the accepted node's window
+ * gathered through win_ref from x and from the slot's history as it stands
+ * before the commit; the caller keeps x (and its stride) unchanged from the
+ * conv call to the commit.  This saves the 3 C floats per node that
+ * gdn_conv_tree_step writes and the commit reads.
+ *   win_ref  [N][3] int32 out (conv) / in (commit); x, x_stride as for conv.
+ * Device errors: as the non-compact calls, plus GDN_DEV_BAD_WINDOW (commit:
+ * a reference of an accepted node outside [-3, N); nothing is written). */
+int gdn_conv_tree_step_compact(const gdn_dims *dims, const float *x, int64_t x_stride,
+                               const float *conv_w, const float *conv_hist,
+                               const int32_t *parents, const int32_t *node_off,
+                               const int32_t *slot_map, float *xc, int32_t *win_ref,
+                               int32_t *status, void *stream);
+
+int gdn_commit_compact(const gdn_dims *dims, const int32_t *accepted, const int32_t *parents,
+                       const int32_t *node_off, const int32_t *slot_map, const float *replay,
+                       int64_t replay_stride, const float *x, int64_t x_stride,
+                       const int32_t *win_ref, float *ssm, float *conv_hist, int32_t *status,
+                       void *stream);
 
 /* Name of a host or device status code ("GDN_OK", "GDN_DEV_DUP_SLOT", ...);
  * "unknown" for any other value.  Never NULL. */

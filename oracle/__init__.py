@@ -92,7 +92,11 @@ class Oracle:
             _P, _P, _P, _P, _P]
         self.lib.gdn_oracle_commit.argtypes = [
             ctypes.POINTER(_Dims), _P, _P, _P, _P, _P, _P, _P, _P]
-        for f in ("gdn_oracle_conv_tree_step", "gdn_oracle_tree_verify", "gdn_oracle_commit"):
+        self.lib.gdn_oracle_window_refs.argtypes = [ctypes.POINTER(_Dims), _P, _P, _P]
+        self.lib.gdn_oracle_commit_compact.argtypes = [
+            ctypes.POINTER(_Dims), _P, _P, _P, _P, _P, _P, ctypes.c_long, _P, _P, _P]
+        for f in ("gdn_oracle_conv_tree_step", "gdn_oracle_tree_verify", "gdn_oracle_commit",
+                  "gdn_oracle_window_refs", "gdn_oracle_commit_compact"):
             getattr(self.lib, f).restype = ctypes.c_int
 
     def conv_tree_step(self, dm: Dims, x, conv_w, conv_hist, parents, node_off, slot_map):
@@ -136,6 +140,30 @@ class Oracle:
             _ptr(ssm), _ptr(conv_hist))
 
 
+    def window_refs(self, dm: Dims, parents, node_off):
+        """Returns (status, refs [N][d_conv - 1] int32): the commit window of every
+        node as references (x row >= 0, or -1 - k for history column k)."""
+        refs = np.zeros((dm.n_nodes, dm.d_conv - 1), dtype=np.int32)
+        cd = dm.c()
+        par, off = _i32(parents), _i32(node_off)
+        rc = self.lib.gdn_oracle_window_refs(ctypes.byref(cd), _ptr(par), _ptr(off), _ptr(refs))
+        return rc, refs
+
+
+    def commit_compact(self, dm: Dims, accepted, parents, node_off, slot_map, replay, x, refs, ssm,
+                        conv_hist):
+        """gdn_oracle_commit with the accepted windows gathered through refs."""
+        assert ssm.dtype == np.float32 and ssm.flags.c_contiguous
+        assert conv_hist.dtype == np.float32 and conv_hist.flags.c_contiguous
+        rep = np.ascontiguousarray(replay, dtype=np.float64)
+        xx = _f32(x)
+        cd = dm.c()
+        acc, par, off, sm, rf = _i32(accepted), _i32(parents), _i32(node_off), _i32(slot_map), _i32(refs)
+        return self.lib.gdn_oracle_commit_compact(
+            ctypes.byref(cd), _ptr(acc), _ptr(par), _ptr(off), _ptr(sm), _ptr(rep), _ptr(xx),
+            xx.shape[1] if xx.ndim == 2 else dm.conv_channels, _ptr(rf), _ptr(ssm), _ptr(conv_hist))
+
+
 _default: Optional[Oracle] = None
 
 
@@ -144,3 +172,4 @@ def get() -> Oracle:
     if _default is None:
         _default = Oracle()
     return _default
+

@@ -278,3 +278,67 @@ int gdn_oracle_commit(const gdn_oracle_dims *dm, const int *accepted, const int 
     free(S);
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------- compact commit windows -- */
+/* The commit window of node t, as references instead of copies: the last K-1
+ * entries of the column sequence P_t = [h_0 .. h_{K-2}, x(root) .. x(t)]
+ * ([P1] the conv tree step also produces the commit window; [P5] column
+ * order: history first, oldest first). */
+int gdn_oracle_window_refs(const gdn_oracle_dims *dm, const int *parents, const int *node_off,
+                           int *refs) {
+    int rc = check_dims(dm);
+    if (rc) return rc;
+    if ((rc = check_offsets(dm, node_off))) return rc;
+    const int K = dm->d_conv;
+    for (int s = 0; s < dm->n_seqs; ++s) {
+        const int n0 = node_off[s], ns = node_off[s + 1] - n0;
+        if ((rc = check_parents(parents, n0, ns))) return rc;
+        int *cols = (int *)malloc(sizeof(int) * (size_t)(K - 1 + ns + 1));
+        int *path = (int *)malloc(sizeof(int) * (size_t)(ns + 1));
+        if (!cols || !path) { free(cols); free(path); return ORACLE_NOMEM; }
+        for (int i = 0; i < ns; ++i) {
+            int m = 0;
+            for (int cur = i; cur >= 0; cur = parents[n0 + cur]) path[m++] = cur;   /* t first */
+            int len = 0;
+            for (int k = 0; k < K - 1; ++k) cols[len++] = -1 - k;                  /* history */
+            for (int j = m - 1; j >= 0; --j) cols[len++] = n0 + path[j];          /* root .. t */
+            for (int j = 0; j < K - 1; ++j) refs[(size_t)(n0 + i) * (K - 1) + j] = cols[len - (K - 1) + j];
+        }
+        free(cols);
+        free(path);
+    }
+    return ORACLE_OK;
+}
+
+/* The commit with referenced windows: every node's window is gathered from x
+ * and the slots' histories as they stand before the commit, then the commit
+ * proceeds exactly as gdn_oracle_commit. */
+int gdn_oracle_commit_compact(const gdn_oracle_dims *dm, const int *accepted, const int *parents,
+                              const int *node_off, const int *slot_map, const double *replay,
+                              const float *x, long x_stride, const int *refs, float *ssm,
+                              float *conv_hist) {
+    int rc = check_dims(dm);
+    if (rc) return rc;
+    if ((rc = check_offsets(dm, node_off))) return rc;
+    const int C = conv_channels(dm), K = dm->d_conv;
+    float *win = (float *)malloc(sizeof(float) * (size_t)(dm->n_nodes > 0 ? dm->n_nodes : 1) * (K - 1) * C);
+    if (!win) return ORACLE_NOMEM;
+    for (int s = 0; s < dm->n_seqs; ++s) {
+        /* only the accepted node's window is needed; indices the commit's own
+           checks would reject are left for them */
+        const int n0 = node_off[s], ns = node_off[s + 1] - n0, slot = slot_map[s], a = accepted[s];
+        if (a < 0 || a >= ns || slot < 0 || slot >= dm->n_slots) continue;
+        for (int j = 0; j < K - 1; ++j) {
+            const int r = refs[(size_t)(n0 + a) * (K - 1) + j];
+            float *dst = win + ((size_t)(n0 + a) * (K - 1) + j) * C;
+            if (r >= 0 && r < dm->n_nodes)
+                memcpy(dst, x + (size_t)r * x_stride, sizeof(float) * (size_t)C);
+            else if (r < 0 && -1 - r < K - 1)
+                memcpy(dst, conv_hist + ((size_t)slot * (K - 1) + (size_t)(-1 - r)) * C, sizeof(float) * (size_t)C);
+            else { free(win); return ORACLE_BAD_NODE_OFF; }
+        }
+    }
+    rc = gdn_oracle_commit(dm, accepted, parents, node_off, slot_map, replay, win, ssm, conv_hist);
+    free(win);
+    return rc;
+}

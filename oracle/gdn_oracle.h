@@ -64,6 +64,21 @@ int gdn_oracle_commit(const gdn_oracle_dims *dm, const int *accepted, const int 
                       const int *node_off, const int *slot_map, const double *replay,
                       const float *win, float *ssm, float *conv_hist);
 
+/* Commit-window references.  The commit window of node t is the last
+ * d_conv-1 columns of P_t = [h_0, ..., h_{d_conv-2}, x(root), ..., x(t)];
+ * refs [N][d_conv-1] names those columns, oldest first: the global node index
+ * of an x row (>= 0), or -1 - k for history column h_k of the slot. */
+int gdn_oracle_window_refs(const gdn_oracle_dims *dm, const int *parents, const int *node_off,
+                           int *refs);
+
+/* gdn_oracle_commit with the window given by references: the window of the
+ * accepted node is gathered from the x rows and the slot's history columns
+ * (as they are before the commit) that refs names. */
+int gdn_oracle_commit_compact(const gdn_oracle_dims *dm, const int *accepted, const int *parents,
+                              const int *node_off, const int *slot_map, const double *replay,
+                              const float *x, long x_stride, const int *refs, float *ssm,
+                              float *conv_hist);
+
 #ifdef __cplusplus
 }
 #endif

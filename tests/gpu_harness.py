@@ -94,16 +94,18 @@ class GpuPools:
 @dataclass
 class GpuOut:
     xc: np.ndarray
-    win: np.ndarray
+    win: Optional[np.ndarray]      # None in the compact form
     o: np.ndarray
     replay: np.ndarray
     status: int
+    win_ref: Optional[np.ndarray] = None   # [N][3] int32, compact form only
 
 
 def run_gpu(b: Batch, pools: GpuPools, q_scale: float = 1.0, commit: bool = True,
             x_pad: int = 0, ba_pad: int = 0, replay_pad: int = 0,
-            xc_override: Optional[np.ndarray] = None) -> GpuOut:
-    """conv -> verify -> commit on the device (pools updated in place)."""
+            xc_override: Optional[np.ndarray] = None, compact: bool = False) -> GpuOut:
+    """conv -> verify -> commit on the device (pools updated in place); with
+    compact=True the windows travel as references (the compact entry points)."""
     C, N, Hv, d = b.C, b.N, b.Hv, b.d
     dm = b.gdims()
     xs = C + x_pad
@@ -123,14 +125,21 @@ def run_gpu(b: Batch, pools: GpuPools, q_scale: float = 1.0, commit: bool = True
     rs = G.gdn_replay_row_floats(d, d) + replay_pad
     o = nan_like((max(N, 1), Hv, d))
     rep = nan_like((max(N, 1), Hv, rs))
-    G.gdn_conv_tree_step(dm, x, xs, w, pools.conv_hist, par, off, sm, xc, win, status)
+    wref = torch.full((max(N, 1), 3), -99, dtype=torch.int32, device="cuda")
+    if compact:
+        G.gdn_conv_tree_step_compact(dm, x, xs, w, pools.conv_hist, par, off, sm, xc, wref, status)
+    else:
+        G.gdn_conv_tree_step(dm, x, xs, w, pools.conv_hist, par, off, sm, xc, win, status)
     xin = xc if xc_override is None else dev(xc_override.astype(np.float32))
     G.gdn_tree_verify(dm, xin, ba, bas, dt, A, pools.ssm, q_scale, par, off, sm, o, rep, rs, status)
-    if commit:
+    if commit and compact:
+        G.gdn_commit_compact(dm, acc, par, off, sm, rep, rs, x, xs, wref, pools.ssm, pools.conv_hist, status)
+    elif commit:
         G.gdn_commit(dm, acc, par, off, sm, rep, rs, win, pools.ssm, pools.conv_hist, status)
     torch.cuda.synchronize()
-    return GpuOut(xc.cpu().numpy()[:N], win.cpu().numpy()[:N], o.cpu().numpy()[:N],
-                  rep.cpu().numpy()[:N, :, : 2 * d + 1], int(status.item()))
+    return GpuOut(xc.cpu().numpy()[:N], None if compact else win.cpu().numpy()[:N], o.cpu().numpy()[:N],
+                  rep.cpu().numpy()[:N, :, : 2 * d + 1], int(status.item()),
+                  wref.cpu().numpy()[:N] if compact else None)
 
 
 @dataclass
@@ -172,7 +181,8 @@ def compare(g: GpuOut, r: OracleOut, tol: float = TOL, check_xc: bool = True):
     errs = {}
     if check_xc:
         errs["xc"] = relerr(g.xc, r.xc)
-        assert np.array_equal(g.win, r.win), "commit windows differ"
+        if g.win is not None:
+            assert np.array_equal(g.win, r.win), "commit windows differ"
     errs["o"] = relerr(g.o, r.o)
     d = g.o.shape[-1] if g.o.size else (g.replay.shape[-1] - 1) // 2
     gp, rp = replay_parts(g.replay, d), replay_parts(r.replay, d)

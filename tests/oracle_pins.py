@@ -392,4 +392,52 @@ def check_tiny_regression(orc):
     assert relerr(ssm[sm[0]], np.array(g["committed_state"])) <= 1e-7
 
 
+# ------------------------------------------------------- compact windows ----
+def check_hand_window_refs(orc):
+    g = _load("hand_window_refs.json")
+    rc, refs = orc.window_refs(_dims(g), g["parents"], g["node_off"])
+    assert rc == 0
+    assert refs.tolist() == g["expected_refs"], refs.tolist()
+
+
+def check_window_refs_gather_windows(orc, seed=51):
+    """Gathering x rows and the slot's history columns through the references
+    gives the conv step's commit windows exactly (trees with several roots,
+    chains, a one-node sequence)."""
+    for kind, sizes in (("tree", [12, 1, 7]), ("chain", [9, 2])):
+        sp, dm, lp, ri, sm = make_case(seed, len(sizes), 1, 2, 16, sizes, kind=kind)
+        parents = ri.parents.copy()
+        if kind == "tree":
+            for s in range(dm.n_seqs):
+                n0 = int(ri.node_off[s])
+                for i in range(5, sizes[s], 5):
+                    parents[n0 + i] = -1
+        rc, xc, win = orc.conv_tree_step(dm, ri.x, lp.conv_w, lp.conv_hist, parents, ri.node_off, sm)
+        assert rc == 0
+        rc, refs = orc.window_refs(dm, parents, ri.node_off)
+        assert rc == 0
+        for s in range(dm.n_seqs):
+            for n in range(int(ri.node_off[s]), int(ri.node_off[s + 1])):
+                for j in range(dm.d_conv - 1):
+                    r = int(refs[n, j])
+                    got = ri.x[r] if r >= 0 else lp.conv_hist[sm[s], -1 - r]
+                    assert np.array_equal(got, win[n, j]), (kind, s, n, j, r)
+
+
+def check_commit_compact_equals_commit(orc, seed=52):
+    """The commit through references leaves both pools bit-identical to the
+    commit with materialised windows."""
+    sp, dm, lp, ri, sm = make_case(seed, 3, 2, 4, 16, [10, 8, 5], P=6)
+    xc, win = _verify_inputs(orc, dm, lp, ri, sm)
+    rc, o, rep = orc.tree_verify(dm, xc, ri.ba, lp.dt_bias, lp.A, lp.ssm, ri.parents, ri.node_off, sm)
+    rc, refs = orc.window_refs(dm, ri.parents, ri.node_off)
+    acc = np.array([0, -1, 4], np.int32)
+    ssm1, hist1 = lp.ssm.copy(), lp.conv_hist.copy()
+    ssm2, hist2 = lp.ssm.copy(), lp.conv_hist.copy()
+    assert orc.commit(dm, acc, ri.parents, ri.node_off, sm, rep, win, ssm1, hist1) == 0
+    assert orc.commit_compact(dm, acc, ri.parents, ri.node_off, sm, rep, ri.x, refs, ssm2, hist2) == 0
+    assert np.array_equal(ssm1, ssm2) and np.array_equal(hist1, hist2)
+    assert not np.array_equal(hist2, lp.conv_hist)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]
