@@ -400,6 +400,82 @@ def time_config(index: int, steps: int, warmup: int, device):
             "gpu_launches_per_step": 4 * sp.layers}
 
 
+def time_decode(steps: int, warmup: int, device):
+    """The plain decode step at the headline shape (64 sequences, one token
+    each, 128-slot pool, 16/32 heads, d = 128), state and history in place."""
+    import torch
+    import gated_deltanet_speculative_gdn_gb300 as G
+    sp = W.Spec("decode64", W.Shape(64, 128, 16, 32, 128), "chain", [1] * 64, 5)
+    sh = sp.shape
+    S, C = sh.n_seqs, sh.conv_channels
+    g = torch.Generator(device=device)
+    g.manual_seed(W.stream_key(sp.seed, 0, W.TID_STATE) & ((1 << 63) - 1))
+    ssm = torch.randn((sh.n_slots, sh.h_v, sh.d, sh.d), generator=g, device=device) * 0.1
+    hist = torch.randn((sh.n_slots, 3, C), generator=g, device=device)
+    lp = W.layer_params(sp, 0, with_pools=False)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    w, dt, A, sm = t(lp.conv_w), t(lp.dt_bias), t(lp.A), t(W.slot_map(sp))
+    nr = 8
+    xs = [torch.randn((S, C), generator=g, device=device) for _ in range(nr)]
+    bas = [t(W.round_inputs(sp, 0, r, with_x=False).ba) for r in range(nr)]
+    xc = torch.empty((S, C), device=device)
+    o = torch.empty((S, sh.h_v, sh.d), device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    dm = G.GdnDims.make(S, S, sh.n_slots, sh.h_k, sh.h_v, sh.d, 16)
+    flush = L2Flush(device)
+
+    def step(i):
+        G.gdn_decode_step(dm, xs[i % nr], C, w, hist, bas[i % nr], 2 * sh.h_v, dt, A, ssm, 1.0, sm, xc, o, status)
+
+    for i in range(warmup):
+        flush(i)
+        step(i)
+    torch.cuda.synchronize()
+    ev = []
+    for i in range(steps):
+        flush(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step(warmup + i)
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    byts = (S * C * 4 + 2 * S * 3 * C * 4 + 16 * C + S * C * 4 + 2 * S * sh.h_v * sh.d * sh.d * 4 +
+            S * 2 * sh.h_v * 4 + S * sh.h_v * sh.d * 4)
+    return {"workload": "64 sequences x 1 token, 128-slot pool, H_k=16, H_v=32, d=128", "ms_per_step": round(ms, 5),
+            "tokens_per_s": round(S / (ms * 1e-3), 1), "algo_bytes": byts,
+            "algo_gbs": round(byts / (ms * 1e-3) / 1e9, 1), "launches_per_step": 3}
+
+
+def time_gated_norm(wl: "DeviceWorkload", steps: int, warmup: int):
+    """The gated RMS norm (sigmoid gate) over the headline verify output."""
+    import torch
+    sh = wl.sp.shape
+    g = torch.Generator(device=wl.device)
+    g.manual_seed(W.stream_key(wl.sp.seed, 0, W.TID_Z) & ((1 << 63) - 1))
+    z = torch.randn((wl.N, sh.h_v * sh.d), generator=g, device=wl.device)
+    nw = torch.ones(sh.d, device=wl.device) + 0.1 * torch.randn(sh.d, generator=g, device=wl.device)
+    y = torch.empty_like(wl.o)
+    flush = L2Flush(wl.device)
+    for i in range(warmup):
+        wl.G.gdn_gated_rmsnorm(wl.dims, wl.o, z, sh.h_v * sh.d, nw, 1e-6, 1, y)
+    torch.cuda.synchronize()
+    ev = []
+    for i in range(steps):
+        flush(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        wl.G.gdn_gated_rmsnorm(wl.dims, wl.o, z, sh.h_v * sh.d, nw, 1e-6, 1, y)
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(x.elapsed_time(b) for x, b in ev)
+    byts = 3 * wl.N * sh.h_v * sh.d * 4 + sh.d * 4
+    return {"ms": round(ms, 5), "algo_bytes": byts, "algo_gbs": round(byts / (ms * 1e-3) / 1e9, 1)}
+
+
 # -------------------------------------------------------------- CPU baseline
 def oracle_sample(variant: str, budget_s: float = 12.0, seqs_per_step=None, first_seq: int = 0, stride: int = 1):
     """Times the oracle (single-threaded C) on whole sequences of the sweep
@@ -556,6 +632,8 @@ def main():
         variants.remove(HEADLINE)
     head = time_variant(HEADLINE, args.steps, args.warmup, device, seed_offset=rank, e2e=True, clocks=True)
     others = {v: time_variant(v, args.steps, args.warmup, device, seed_offset=rank) for v in variants}
+    extra = {"decode_step": time_decode(args.steps, args.warmup, device),
+             "gated_rmsnorm_headline": time_gated_norm(head["wl"], args.steps, args.warmup)}
     cfg_ids = [] if args.configs in ("", "none") else [int(c) for c in args.configs.split(",")]
     configs = {W.SPEC_NAMES[c]: time_config(c, min(args.steps, 20), args.warmup, device) for c in cfg_ids}
 
@@ -653,6 +731,7 @@ def main():
         "cpu_baseline": cpu,
         "parity_spot": spot,
         "configs": configs,
+        "other_stages": extra,
     }
     print(json.dumps(line))
     if dist is not None:

@@ -25,13 +25,14 @@ LIB_PATH = os.path.join(_HERE, "libgdn_gb300.so")
 
 GDN_OK = 0
 GDN_ERR_NULL, GDN_ERR_DIMS, GDN_ERR_STRIDE, GDN_ERR_ALIGN = -1, -2, -3, -4
-GDN_ERR_ALIAS, GDN_ERR_LAUNCH, GDN_ERR_TMA = -5, -6, -7
+GDN_ERR_ALIAS, GDN_ERR_LAUNCH, GDN_ERR_TMA, GDN_ERR_ARG = -5, -6, -7, -8
 GDN_DEV_BAD_NODE_OFF, GDN_DEV_BAD_PARENT, GDN_DEV_BAD_SLOT = 1, 2, 3
 GDN_DEV_DUP_SLOT, GDN_DEV_BAD_ACCEPTED, GDN_DEV_TIMEOUT = 4, 5, 6
 GDN_DEV_BAD_WINDOW = 7
 
 EXPORTED_SYMBOLS = ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit",
-                    "gdn_conv_tree_step_compact", "gdn_commit_compact",
+                    "gdn_conv_tree_step_compact", "gdn_commit_compact", "gdn_gated_rmsnorm",
+                    "gdn_decode_step",
                     "gdn_status_str", "gdn_replay_row_floats")
 
 if not os.path.exists(LIB_PATH):
@@ -71,8 +72,11 @@ lib.gdn_tree_verify.argtypes = [_DP, _P, _P, _I64, _P, _P, _P, ctypes.c_float, _
 lib.gdn_commit.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P]
 lib.gdn_conv_tree_step_compact.argtypes = [_DP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 lib.gdn_commit_compact.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _P]
+lib.gdn_gated_rmsnorm.argtypes = [_DP, _P, _P, _I64, _P, ctypes.c_float, ctypes.c_int, _P, _P]
+lib.gdn_decode_step.argtypes = [_DP, _P, _I64, _P, _P, _P, _I64, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
+                                _P]
 for _f in ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit", "gdn_conv_tree_step_compact",
-           "gdn_commit_compact"):
+           "gdn_commit_compact", "gdn_gated_rmsnorm", "gdn_decode_step"):
     getattr(lib, _f).restype = ctypes.c_int
 lib.gdn_status_str.argtypes = [ctypes.c_int]
 lib.gdn_status_str.restype = ctypes.c_char_p
@@ -157,3 +161,18 @@ def gdn_commit_compact(dims: GdnDims, accepted, parents, node_off, slot_map, rep
                                 _ptr(slot_map), _ptr(replay), int(replay_stride), _ptr(x), int(x_stride),
                                 _ptr(win_ref), _ptr(ssm), _ptr(conv_hist), _ptr(status), _stream(stream))
     return _check("gdn_commit_compact", rc, raise_on_error)
+
+
+def gdn_gated_rmsnorm(dims: GdnDims, o, z, z_stride: int, norm_w, eps: float, gate_mode: int, y,
+                      stream=None, raise_on_error: bool = True) -> int:
+    rc = lib.gdn_gated_rmsnorm(ctypes.byref(dims), _ptr(o), _ptr(z), int(z_stride), _ptr(norm_w), float(eps),
+                               int(gate_mode), _ptr(y), _stream(stream))
+    return _check("gdn_gated_rmsnorm", rc, raise_on_error)
+
+
+def gdn_decode_step(dims: GdnDims, x, x_stride: int, conv_w, conv_hist, ba, ba_stride: int, dt_bias, A, ssm,
+                    q_scale: float, slot_map, xc, o, status, stream=None, raise_on_error: bool = True) -> int:
+    rc = lib.gdn_decode_step(ctypes.byref(dims), _ptr(x), int(x_stride), _ptr(conv_w), _ptr(conv_hist), _ptr(ba),
+                             int(ba_stride), _ptr(dt_bias), _ptr(A), _ptr(ssm), float(q_scale), _ptr(slot_map),
+                             _ptr(xc), _ptr(o), _ptr(status), _stream(stream))
+    return _check("gdn_decode_step", rc, raise_on_error)

@@ -12,6 +12,7 @@ extern "C" const char *gdn_status_str(int code) {
         case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS";
         case GDN_ERR_LAUNCH: return "GDN_ERR_LAUNCH";
         case GDN_ERR_TMA: return "GDN_ERR_TMA";
+        case GDN_ERR_ARG: return "GDN_ERR_ARG";
         case GDN_DEV_BAD_NODE_OFF: return "GDN_DEV_BAD_NODE_OFF";
         case GDN_DEV_BAD_PARENT: return "GDN_DEV_BAD_PARENT";
         case GDN_DEV_BAD_SLOT: return "GDN_DEV_BAD_SLOT";

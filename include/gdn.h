@@ -98,7 +98,8 @@ enum {
     GDN_ERR_ALIGN = -4,        /* a float pointer is not 16-byte aligned          */
     GDN_ERR_ALIAS = -5,        /* an output overlaps an input or another output  */
     GDN_ERR_LAUNCH = -6,       /* the CUDA launch failed (cudaGetLastError)       */
-    GDN_ERR_TMA = -7           /* the TMA descriptor of the state pool failed     */
+    GDN_ERR_TMA = -7,          /* the TMA descriptor of the state pool failed     */
+    GDN_ERR_ARG = -8           /* an argument outside its allowed values          */
 };
 
 /* device-side codes written to *status */
@@ -208,6 +209,44 @@ int gdn_commit_compact(const gdn_dims *dims, const int32_t *accepted, const int3
                        int64_t replay_stride, const float *x, int64_t x_stride,
                        const int32_t *win_ref, float *ssm, float *conv_hist, int32_t *status,
                        void *stream);
+
+/* Gated RMS norm, the output stage after the recurrence (TensorSharp PR #175,
+ * the Qwen 3.5 / Qwen4Exp GDN block: gated delta net -> gated norm; the output
+ * gate is a SiLU, gate_mode 0, or a sigmoid, gate_mode 1).  For node t, value
+ * head h and i < d:
+ *     y[t][h][i] = o[t][h][i] / sqrt(mean_i(o[t][h][.]^2) + eps) * norm_w[i]
+ *                  * gate(z[t][h d + i])
+ *   o       [N][H_v][d] in (e.g. gdn_tree_verify's output)
+ *   z       [N][z_stride] in, z_stride >= H_v d and % 4 == 0
+ *   norm_w  [d] in (one weight vector shared by the heads)
+ *   eps     >= 0 (eps = 0 with an all-zero head gives NaN)
+ *   y       [N][H_v][d] out (must not overlap the inputs)
+ * Host errors: GDN_ERR_ARG for gate_mode outside {0, 1} or eps < 0 / not
+ * finite.  No device errors. */
+int gdn_gated_rmsnorm(const gdn_dims *dims, const float *o, const float *z, int64_t z_stride,
+                      const float *norm_w, float eps, int gate_mode, float *y, void *stream);
+
+/* Plain decode step (TensorSharp PR #175: a step without speculation commits
+ * its post-window state at once, the caller's "slot -1"; lucebox PR #625:
+ * ggml_ssm_conv_step with in-place history write-back and the raw-gate gated
+ * delta net in place).  One token per sequence: dims->n_nodes must equal
+ * dims->n_seqs and token s belongs to sequence s.  For each s, with
+ * h = conv_hist[slot_map[s]] and the column sequence P = [h_0, h_1, h_2, x_s]:
+ *     xc[s][c] = SiLU(sum_{j=0..3} P[j][c] conv_w[c][j]);   h <- [h_1, h_2, x_s]
+ * and for every value head h with the gates and normalised q/k of
+ * gdn_tree_verify:
+ *     S <- decay S;  u = beta (v - S k^);  S <- S + u k^T;  o[s][h] = q_scale S q^
+ * on ssm[slot_map[s]][h] in place.  This is gdn_conv_tree_step +
+ * gdn_tree_verify + gdn_commit on one-node trees with every node accepted,
+ * without the windows and replay rows.
+ *   x [S][x_stride] in; conv_w in; conv_hist, ssm in/out; ba [S][ba_stride] in;
+ *   dt_bias, A in; slot_map [S] in; xc [S][C] out; o [S][H_v][d] out.
+ * Device errors: GDN_DEV_BAD_SLOT, GDN_DEV_DUP_SLOT (two sequences in one
+ * slot); on any error (or a non-zero *status on entry) nothing is written. */
+int gdn_decode_step(const gdn_dims *dims, const float *x, int64_t x_stride, const float *conv_w,
+                    float *conv_hist, const float *ba, int64_t ba_stride, const float *dt_bias,
+                    const float *A, float *ssm, float q_scale, const int32_t *slot_map, float *xc,
+                    float *o, int32_t *status, void *stream);
 
 /* Name of a host or device status code ("GDN_OK", "GDN_DEV_DUP_SLOT", ...);
  * "unknown" for any other value.  Never NULL. */

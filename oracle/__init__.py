@@ -95,8 +95,14 @@ class Oracle:
         self.lib.gdn_oracle_window_refs.argtypes = [ctypes.POINTER(_Dims), _P, _P, _P]
         self.lib.gdn_oracle_commit_compact.argtypes = [
             ctypes.POINTER(_Dims), _P, _P, _P, _P, _P, _P, ctypes.c_long, _P, _P, _P]
+        self.lib.gdn_oracle_gated_rmsnorm.argtypes = [
+            ctypes.POINTER(_Dims), _P, _P, ctypes.c_long, _P, ctypes.c_double, ctypes.c_int, _P]
+        self.lib.gdn_oracle_decode_step.argtypes = [
+            ctypes.POINTER(_Dims), _P, ctypes.c_long, _P, _P, _P, ctypes.c_long, _P, _P, _P, ctypes.c_double,
+            _P, _P, _P]
         for f in ("gdn_oracle_conv_tree_step", "gdn_oracle_tree_verify", "gdn_oracle_commit",
-                  "gdn_oracle_window_refs", "gdn_oracle_commit_compact"):
+                  "gdn_oracle_window_refs", "gdn_oracle_commit_compact", "gdn_oracle_gated_rmsnorm",
+                  "gdn_oracle_decode_step"):
             getattr(self.lib, f).restype = ctypes.c_int
 
     def conv_tree_step(self, dm: Dims, x, conv_w, conv_hist, parents, node_off, slot_map):
@@ -162,6 +168,31 @@ class Oracle:
         return self.lib.gdn_oracle_commit_compact(
             ctypes.byref(cd), _ptr(acc), _ptr(par), _ptr(off), _ptr(sm), _ptr(rep), _ptr(xx),
             xx.shape[1] if xx.ndim == 2 else dm.conv_channels, _ptr(rf), _ptr(ssm), _ptr(conv_hist))
+
+    def gated_rmsnorm(self, dm: Dims, o, z, w, eps: float, gate_mode: int):
+        """Returns (status, y [N][h_v][d] float64)."""
+        oo, zz, ww = _f32(o), _f32(z), _f32(w)
+        y = np.zeros((dm.n_nodes, dm.h_v, dm.d), dtype=np.float64)
+        cd = dm.c()
+        rc = self.lib.gdn_oracle_gated_rmsnorm(ctypes.byref(cd), _ptr(oo), _ptr(zz),
+                                               zz.shape[1] if zz.ndim == 2 else dm.h_v * dm.d, _ptr(ww),
+                                               float(eps), int(gate_mode), _ptr(y))
+        return rc, y
+
+    def decode_step(self, dm: Dims, x, conv_w, conv_hist, ba, dt_bias, A, ssm, slot_map, q_scale: float = 1.0):
+        """One token per sequence, in place into ``ssm`` and ``conv_hist``
+        (float32, C-contiguous).  Returns (status, xc [S][C], o [S][h_v][d])."""
+        assert ssm.dtype == np.float32 and ssm.flags.c_contiguous
+        assert conv_hist.dtype == np.float32 and conv_hist.flags.c_contiguous
+        xx, bb = _f32(x), _f32(ba)
+        xc = np.zeros((dm.n_seqs, dm.conv_channels), dtype=np.float64)
+        o = np.zeros((dm.n_seqs, dm.h_v, dm.d), dtype=np.float64)
+        cd = dm.c()
+        w, dt, Aa, sm = _f32(conv_w), _f32(dt_bias), _f32(A), _i32(slot_map)
+        rc = self.lib.gdn_oracle_decode_step(
+            ctypes.byref(cd), _ptr(xx), xx.shape[1], _ptr(w), _ptr(conv_hist), _ptr(bb), bb.shape[1], _ptr(dt),
+            _ptr(Aa), _ptr(ssm), float(q_scale), _ptr(sm), _ptr(xc), _ptr(o))
+        return rc, xc, o
 
 
 _default: Optional[Oracle] = None

@@ -342,3 +342,112 @@ int gdn_oracle_commit_compact(const gdn_oracle_dims *dm, const int *accepted, co
     free(win);
     return rc;
 }
+
+/* ------------------------------------------------------ gated RMS norm ---- */
+/* TensorSharp PR #175, the Qwen 3.5 / Qwen4Exp GDN block: the recurrence's
+ * output goes through a gated norm before the scatter; the output gate is a
+ * SiLU (gate_mode 0, the existing callers) or a sigmoid (gate_mode 1).  The
+ * norm is an RMS norm over the d values of one head with a per-channel weight,
+ * then the gate of z multiplies element by element. */
+int gdn_oracle_gated_rmsnorm(const gdn_oracle_dims *dm, const float *o, const float *z, long z_stride,
+                             const float *w, double eps, int gate_mode, double *y) {
+    int rc = check_dims(dm);
+    if (rc) return rc;
+    if (gate_mode != 0 && gate_mode != 1) return ORACLE_BAD_DIMS;
+    const int d = dm->d, Hv = dm->h_v;
+    for (int t = 0; t < dm->n_nodes; ++t)
+        for (int h = 0; h < Hv; ++h) {
+            const float *orow = o + ((size_t)t * Hv + h) * d;
+            const float *zrow = z + (size_t)t * z_stride + (size_t)h * d;
+            double ss = 0.0;
+            for (int i = 0; i < d; ++i) ss += (double)orow[i] * (double)orow[i];
+            const double inv = 1.0 / sqrt(ss / d + eps);
+            for (int i = 0; i < d; ++i) {
+                const double g = gate_mode == 0 ? silu((double)zrow[i]) : sigmoid((double)zrow[i]);
+                y[((size_t)t * Hv + h) * d + i] = (double)orow[i] * inv * (double)w[i] * g;
+            }
+        }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------- decode step ---- */
+/* TensorSharp PR #175: a step without speculation has nothing to decide later,
+ * so its post-window state is committed at once (the caller's "slot -1");
+ * lucebox PR #625: ggml_ssm_conv_step (history window + SiLU(conv) + in-place
+ * history write-back) and the raw-gate gated delta net in place.  The step is
+ * the gated delta rule of [GDN] for one token, state and history updated in
+ * the slot. */
+int gdn_oracle_decode_step(const gdn_oracle_dims *dm, const float *x, long x_stride, const float *conv_w,
+                           float *conv_hist, const float *ba, long ba_stride, const float *dt_bias,
+                           const float *A, float *ssm, double q_scale, const int *slot_map, double *xc,
+                           double *o) {
+    int rc = check_dims(dm);
+    if (rc) return rc;
+    const int C = conv_channels(dm), K = dm->d_conv, d = dm->d, Hk = dm->h_k, Hv = dm->h_v, G = Hv / Hk;
+    const size_t dd = (size_t)d * d;
+    for (int s = 0; s < dm->n_seqs; ++s) {
+        const int slot = slot_map[s];
+        if (slot < 0 || slot >= dm->n_slots) return ORACLE_BAD_SLOT;
+        for (int s2 = 0; s2 < s; ++s2)
+            if (slot_map[s2] == slot) return ORACLE_DUP_SLOT;
+    }
+    double *qn = (double *)malloc(sizeof(double) * (size_t)d);
+    double *kn = (double *)malloc(sizeof(double) * (size_t)d);
+    double *S = (double *)malloc(sizeof(double) * dd);
+    if (!qn || !kn || !S) { free(qn); free(kn); free(S); return ORACLE_NOMEM; }
+    for (int s = 0; s < dm->n_seqs; ++s) {
+        const int slot = slot_map[s];
+        float *hist = conv_hist + (size_t)slot * (K - 1) * C;
+        const float *xs = x + (size_t)s * x_stride;
+        double *xcs = xc + (size_t)s * C;
+        /* conv over the column sequence [h_0 .. h_{K-2}, x_s], taps oldest first */
+        for (int c = 0; c < C; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < K; ++j) {
+                const float col = j < K - 1 ? hist[(size_t)j * C + c] : xs[c];
+                acc += (double)col * (double)conv_w[(size_t)c * K + j];
+            }
+            xcs[c] = silu(acc);
+        }
+        /* the history becomes the last K - 1 columns */
+        for (int c = 0; c < C; ++c) {
+            for (int j = 0; j < K - 2; ++j) hist[(size_t)j * C + c] = hist[(size_t)(j + 1) * C + c];
+            hist[(size_t)(K - 2) * C + c] = xs[c];
+        }
+        for (int h = 0; h < Hv; ++h) {
+            const int kh = h / G;
+            const double *q = xcs + (size_t)kh * d, *k = xcs + (size_t)Hk * d + (size_t)kh * d;
+            const double *v = xcs + (size_t)2 * Hk * d + (size_t)h * d;
+            /* the recurrence reads the conv output at the boundary precision
+               (fp32), as the tree path's verify does */
+            double sq = 0.0, sk = 0.0;
+            for (int c = 0; c < d; ++c) {
+                const double qf = (double)(float)q[c], kf = (double)(float)k[c];
+                sq += qf * qf;
+                sk += kf * kf;
+            }
+            for (int c = 0; c < d; ++c) {
+                qn[c] = (double)(float)q[c] / sqrt(sq + L2_EPS);
+                kn[c] = (double)(float)k[c] / sqrt(sk + L2_EPS);
+            }
+            const double beta = sigmoid((double)ba[(size_t)s * ba_stride + h]);
+            const double decay = exp(softplus((double)ba[(size_t)s * ba_stride + Hv + h] + (double)dt_bias[h]) *
+                                     (double)A[h]);
+            float *Sf = ssm + ((size_t)slot * Hv + h) * dd;
+            for (size_t e = 0; e < dd; ++e) S[e] = decay * (double)Sf[e];
+            double *orow = o + ((size_t)s * Hv + h) * d;
+            for (int r = 0; r < d; ++r) {
+                double skr = 0.0;
+                for (int c = 0; c < d; ++c) skr += S[(size_t)r * d + c] * kn[c];
+                const double u = beta * ((double)(float)v[r] - skr);
+                for (int c = 0; c < d; ++c) S[(size_t)r * d + c] += u * kn[c];
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += S[(size_t)r * d + c] * qn[c];
+                orow[r] = q_scale * acc;
+            }
+            for (size_t e = 0; e < dd; ++e) Sf[e] = (float)S[e];
+        }
+    }
+    free(qn); free(kn); free(S);
+    return ORACLE_OK;
+}

@@ -79,6 +79,26 @@ int gdn_oracle_commit_compact(const gdn_oracle_dims *dm, const int *accepted, co
                               const float *x, long x_stride, const int *refs, float *ssm,
                               float *conv_hist);
 
+/* Gated RMS norm of the verify output (the output stage after the
+ * recurrence): for node t, value head h and i < d,
+ *     y[t][h][i] = o[t][h][i] / sqrt(mean_i o[t][h][.]^2 + eps) * w[i] * gate(z[t][h d + i])
+ * with gate = SiLU (gate_mode 0) or sigmoid (gate_mode 1).
+ * o [N][h_v][d] float, z [N][z_stride] float, w [d] float; y [N][h_v][d] double. */
+int gdn_oracle_gated_rmsnorm(const gdn_oracle_dims *dm, const float *o, const float *z, long z_stride,
+                             const float *w, double eps, int gate_mode, double *y);
+
+/* Plain decode step: one token per sequence (token s belongs to sequence s),
+ * the state and the conv history of its slot advanced in place.  The token
+ * is the only node of a one-node tree, accepted at once:
+ *     P = [h_0 .. h_{d_conv-2}, x_s],  xc = SiLU(sum_j P[j] w[j]),  h <- last d_conv-1 of P
+ *     S <- decay S;  u = beta (v - S k^);  S <- S + u k^T;  o = q_scale S q^
+ * x [S][x_stride], ba [S][ba_stride]; ssm, conv_hist in/out; out xc [S][C]
+ * (double) and o [S][h_v][d] (double).  Slots must be distinct. */
+int gdn_oracle_decode_step(const gdn_oracle_dims *dm, const float *x, long x_stride, const float *conv_w,
+                           float *conv_hist, const float *ba, long ba_stride, const float *dt_bias,
+                           const float *A, float *ssm, double q_scale, const int *slot_map, double *xc,
+                           double *o);
+
 #ifdef __cplusplus
 }
 #endif

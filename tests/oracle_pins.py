@@ -440,4 +440,119 @@ def check_commit_compact_equals_commit(orc, seed=52):
     assert not np.array_equal(hist2, lp.conv_hist)
 
 
+# ------------------------------------------------------- gated RMS norm ----
+def check_hand_gated_norm(orc):
+    g = _load("hand_gated_norm.json")
+    dm = O.Dims(1, 1, 1, 1, 1, 2)
+    for c in g["cases"]:
+        rc, y = orc.gated_rmsnorm(dm, np.array([[c["o"]]], np.float32), np.array([c["z"]], np.float32),
+                                  np.array(c["w"], np.float32), c["eps"], c["gate_mode"])
+        assert rc == 0
+        assert np.max(np.abs(y[0, 0] - np.array(c["expected_y"]))) <= g["tolerance_abs"], (c, y)
+
+
+def _norm_case(seed, N=5, Hv=3, d=16):
+    st = W.Stream(seed, 0, 99)
+    o = st.normal(N * Hv * d).reshape(N, Hv, d)
+    z = st.normal(N * Hv * d, 2.0).reshape(N, Hv * d)
+    w = st.normal(d, 0.5)
+    return O.Dims(1, N, 1, 1, Hv, d), o, z, w
+
+
+def check_gated_norm_constant_head(orc, seed=61):
+    """A head whose outputs all equal c normalises to c / sqrt(c^2 + eps)."""
+    dm, o, z, w = _norm_case(seed)
+    o[:] = np.float32(-1.5)
+    eps = 0.25
+    for mode, gate in ((0, lambda v: v / (1 + np.exp(-v))), (1, lambda v: 1 / (1 + np.exp(-v)))):
+        rc, y = orc.gated_rmsnorm(dm, o, z, w, eps, mode)
+        want = (-1.5 / np.sqrt(2.25 + eps)) * w.astype(np.float64) * gate(z.astype(np.float64).reshape(y.shape))
+        assert relerr(y, want) <= TIGHT
+
+
+def check_gated_norm_modes_relation(orc, seed=62):
+    """SiLU(z) = z sigmoid(z), so the SiLU-gated output is z times the
+    sigmoid-gated one, element by element."""
+    dm, o, z, w = _norm_case(seed)
+    rc0, ys = orc.gated_rmsnorm(dm, o, z, w, 1e-6, 0)
+    rc1, yg = orc.gated_rmsnorm(dm, o, z, w, 1e-6, 1)
+    assert rc0 == rc1 == 0
+    assert relerr(ys, z.astype(np.float64).reshape(yg.shape) * yg) <= TIGHT
+
+
+def check_gated_norm_scale_invariance(orc, seed=63):
+    """With eps = 0 the norm removes any power-of-two scale of o exactly."""
+    dm, o, z, w = _norm_case(seed)
+    rc, y1 = orc.gated_rmsnorm(dm, o, z, w, 0.0, 1)
+    rc, y2 = orc.gated_rmsnorm(dm, (o * np.float32(2.0 ** 20)).astype(np.float32), z, w, 0.0, 1)
+    assert relerr(y1, y2) <= TIGHT
+    rc, y3 = orc.gated_rmsnorm(dm, o, z, w, 0.0, 2)
+    assert rc != 0
+
+
+# ---------------------------------------------------------- decode step ----
+def _decode_case(seed, S=3, Hk=2, Hv=4, d=16, P=5):
+    sp = W.Spec(f"dec{seed}", W.Shape(S, P, Hk, Hv, d), "chain", [1] * S, seed)
+    lp = W.layer_params(sp)
+    ri = W.round_inputs(sp)
+    sm = W.slot_map(sp)
+    return sp, O.Dims(S, S, P, Hk, Hv, d), lp, ri, sm
+
+
+def check_decode_step_is_one_node_tree_committed(orc, seed=71):
+    """A decode step equals the tree path on one-node trees with the node
+    accepted: same xc and o, same state and history afterwards."""
+    sp, dm, lp, ri, sm = _decode_case(seed)
+    ssm, hist = lp.ssm.copy(), lp.conv_hist.copy()
+    rc, xc, o = orc.decode_step(dm, ri.x, lp.conv_w, hist, ri.ba, lp.dt_bias, lp.A, ssm, sm, q_scale=0.5)
+    assert rc == 0
+    xcf, win = _verify_inputs(orc, dm, lp, ri, sm)
+    rc, o2, rep = orc.tree_verify(dm, xcf, ri.ba, lp.dt_bias, lp.A, lp.ssm, ri.parents, ri.node_off, sm,
+                                  q_scale=0.5)
+    ssm2, hist2 = lp.ssm.copy(), lp.conv_hist.copy()
+    assert orc.commit(dm, np.zeros(dm.n_seqs, np.int32), ri.parents, ri.node_off, sm, rep, win, ssm2, hist2) == 0
+    rc, xc2, _ = orc.conv_tree_step(dm, ri.x, lp.conv_w, lp.conv_hist, ri.parents, ri.node_off, sm)
+    assert relerr(xc, xc2) <= TIGHT
+    assert relerr(o, o2) <= TIGHT
+    assert np.array_equal(hist, hist2)
+    # the committed state rounds once to fp32 on both paths
+    assert relerr(ssm, ssm2) <= 1e-6
+
+
+def check_decode_steps_match_literal_decode(orc, seed=72, steps=5):
+    """Several decode steps equal the literal matrix form S (I - beta k k^T)
+    + beta v k^T applied token by token, with the conv as a correlation over
+    the history and the tokens so far."""
+    sp, dm, lp, ri, sm = _decode_case(seed, S=2)
+    ssm, hist = lp.ssm.copy(), lp.conv_hist.copy()
+    xs, bas, outs = [], [], []
+    for r in range(steps):
+        ri = W.round_inputs(sp, 0, r)
+        rc, xc, o = orc.decode_step(dm, ri.x, lp.conv_w, hist, ri.ba, lp.dt_bias, lp.A, ssm, sm)
+        assert rc == 0
+        xs.append(ri.x)
+        bas.append(ri.ba)
+        outs.append(o)
+    for s in range(dm.n_seqs):
+        slot = sm[s]
+        toks = np.stack([x[s] for x in xs])
+        _, act, w3 = conv_path(lp.conv_hist[slot], toks, lp.conv_w)
+        assert np.array_equal(hist[slot], w3.astype(np.float32))
+        for h in range(dm.h_v):
+            S, o = decode_path(lp.ssm[slot, h], act.astype(np.float32), np.stack([b[s] for b in bas]),
+                               lp.dt_bias[h], lp.A[h], dm.h_k, dm.h_v, dm.d, h)
+            assert relerr(np.stack([out[s, h] for out in outs]), o) <= 1e-5, (s, h)
+            assert relerr(ssm[slot, h], S) <= 1e-5, (s, h)
+
+
+def check_decode_step_rejects_shared_slots(orc, seed=73):
+    sp, dm, lp, ri, sm = _decode_case(seed)
+    sm = sm.copy()
+    sm[2] = sm[0]
+    ssm, hist = lp.ssm.copy(), lp.conv_hist.copy()
+    rc, _, _ = orc.decode_step(dm, ri.x, lp.conv_w, hist, ri.ba, lp.dt_bias, lp.A, ssm, sm)
+    assert rc == O.DUP_SLOT
+    assert np.array_equal(ssm, lp.ssm) and np.array_equal(hist, lp.conv_hist)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

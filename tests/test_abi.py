@@ -151,3 +151,34 @@ def test_empty_batches_are_no_ops():
     d = dims(n_nodes=0)
     assert conv(d) == G.GDN_OK
     assert verify(d) == G.GDN_OK
+
+
+def test_gated_norm_host_validation():
+    d = dims()
+    base = dict(o=FAKE, z=FAKE * 2, z_stride=d.h_v * d.d_v, w=FAKE * 3, eps=1e-6, mode=0, y=FAKE * 4)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return G.gdn_gated_rmsnorm(d, a["o"], a["z"], a["z_stride"], a["w"], a["eps"], a["mode"], a["y"],
+                                   stream=0, raise_on_error=False)
+
+    assert call(mode=2) == G.GDN_ERR_ARG
+    assert call(eps=-1.0) == G.GDN_ERR_ARG
+    assert call(eps=float("nan")) == G.GDN_ERR_ARG
+    assert call(z_stride=d.h_v * d.d_v - 4) == G.GDN_ERR_STRIDE
+    assert call(o=None) == G.GDN_ERR_NULL
+    assert call(y=FAKE + 4) == G.GDN_ERR_ALIGN
+    assert call(y=FAKE) == G.GDN_ERR_ALIAS
+
+
+def test_compact_host_validation():
+    d = dims()
+    C = d.conv_channels
+    assert G.gdn_conv_tree_step_compact(d, FAKE, C, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6,
+                                        FAKE * 7, None, FAKE * 9, stream=0, raise_on_error=False) == G.GDN_ERR_NULL
+    rs = G.gdn_replay_row_floats(d.d_k, d.d_v)
+    assert G.gdn_commit_compact(d, FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, rs, FAKE * 6, C - 4, FAKE * 7,
+                                FAKE * 8, FAKE * 9, FAKE * 10, stream=0, raise_on_error=False) == G.GDN_ERR_STRIDE
+    assert G.gdn_commit_compact(d, FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, rs, FAKE * 6, C, None,
+                                FAKE * 8, FAKE * 9, FAKE * 10, stream=0, raise_on_error=False) == G.GDN_ERR_NULL

@@ -26,8 +26,8 @@ _UPDATE = (f"{I16}for (int r = 0; r < d; ++r)\n"
 # (what the mistake is, correct passage, planted passage)
 MUTANTS = [
     ("conv taps reversed",
-     "(double)conv_w[(size_t)c * K + j];",
-     "(double)conv_w[(size_t)c * K + (K - 1 - j)];"),
+     "acc += (double)col[K - 1 - j][c] * (double)conv_w[(size_t)c * K + j];",
+     "acc += (double)col[K - 1 - j][c] * (double)conv_w[(size_t)c * K + (K - 1 - j)];"),
     ("history order flipped",
      "col[b] = hist + (size_t)(K - 2 - above) * C;",
      "col[b] = hist + (size_t)above * C;"),
@@ -41,7 +41,7 @@ MUTANTS = [
      "S0[(size_t)r * d + c] = S0f[(size_t)r * d + c];",
      "S0[(size_t)r * d + c] = S0f[(size_t)c * d + r];"),
     ("grouped heads mapped h mod H_k",
-     "const int kh = h / G;",
+     "const int kh = h / G;                  /* [P3] q/k heads broadcast */",
      "const int kh = h % Hk;"),
     ("output read before the rank-one update",
      _UPDATE + _O_LOOP,
