@@ -472,7 +472,7 @@ constexpr int kIssueGram = 1, kIssueHi = 2;       // MMA issuer warps (warp 3 is
 constexpr int kTeam0 = 4;                          // team t: warps 4 + 4t .. 7 + 4t
 constexpr int kSplit0 = 12, kSplitThreads = 128;   // splitter warps 12-15
 constexpr int kMaxItems = 64;                      // items per CTA
-constexpr int NR = 9;                              // S0 ring depth (K-chunks)
+constexpr int NR = 6;                              // S0 ring depth (K-chunks)
 constexpr int kPrefetch = 2;                       // items whose state is requested into L2 ahead
 constexpr uint32_t kChunk = 128 * 128;             // one S0 K-chunk: 128 rows x 32 fp32
 constexpr uint32_t kBChunk = 64 * 128;             // one B K-chunk: rows 0-15 k, 16-31 q, 32-63 their lo
@@ -480,7 +480,9 @@ constexpr uint32_t kBTeam = 4 * kBChunk;           // one team's B
 constexpr uint32_t kQKBox = 16 * 128;              // 16 rows of k or q, one K-chunk
 constexpr uint32_t RAW = 0;
 constexpr uint32_t BT = RAW + NR * kChunk;         // per team
-constexpr uint32_t SMALL = BT + 2 * kBTeam;
+constexpr uint32_t kStage = 16 * D * 4;            // one [16 nodes][d] output tile
+constexpr uint32_t STG = BT + 2 * kBTeam;          // per team: o | k^ | u tiles for TMA stores
+constexpr uint32_t SMALL = STG + 2 * 3 * kStage;
 // per-team small area (4-byte words), [16][16] matrices:
 //   KA + KB = k_t . k_j and QA + QB = q_t . k_j (Gram partial sums from the
 //   hi and lo rows, row t); GM = gamma_{j->t} (row t; 1 on the diagonal, 0
@@ -551,6 +553,7 @@ __device__ __forceinline__ float4 lo4(float4 x) {
 
 __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     tree_verify_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap xmap,
+                          const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap rmap,
                           const VerifyArgs a) {
     using namespace wsv;
     extern __shared__ unsigned char smem_raw[];
@@ -747,6 +750,9 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         float *gsk = tws + T_GSK, *gsq = tws + T_GSQ, *rk_s = tws + T_RK, *gam_s = tws + T_GAM;
         int *par = reinterpret_cast<int *>(tws + T_PAR);
         unsigned char *bt_t = sb + BT + team * kBTeam;
+        // output tiles of a full (16-node) item, written by TMA stores
+        float *stg_o = reinterpret_cast<float *>(sb + STG + team * 3 * kStage);
+        float *stg_k = stg_o + kSeg * D, *stg_u = stg_k + kSeg * D;
 
         // parents and gate inputs of the team's next item, loaded one item ahead
         int p_nx = -1;
@@ -810,7 +816,9 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             const int voff = 2 * a.Hk * D + h * D;
             int p = p_nx;
             const float bv = bv_nx, av = av_nx, dtb = dtb_nx, Ah = ah_nx;
-            // the team's previous epilogue has finished reading the small area
+            // the previous item's output stores have read the tiles; the team's
+            // previous epilogue has finished reading the small area
+            if (ttid == 0) gdn::bulk_wait_read0();
             team_sync(team);
 
             // ---- A: parents and gates (warp 0 of the team: lane = node) -----------
@@ -916,12 +924,19 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
 
             // ---- D: the replay rows' k^ and this thread's v ----------------------
             // replay: k^ of this warp's nodes, from B's raw rows
+            const bool full = lc == kSeg;  // all 16 rows of the tiles belong to this sequence
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int t = tw + 4 * m;
-                if (t < lc && staged)
-                    *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride + 4 * lane) =
-                        scale4(*reinterpret_cast<const float4 *>(bt_t + sw_off(t, 4 * lane, kBChunk)), rk_s[t]);
+                if (t < lc && staged) {
+                    const float4 kh = scale4(*reinterpret_cast<const float4 *>(bt_t + sw_off(t, 4 * lane, kBChunk)),
+                                             rk_s[t]);
+                    if (full)
+                        *reinterpret_cast<float4 *>(stg_k + t * D + 4 * lane) = kh;
+                    else
+                        *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride +
+                                                    4 * lane) = kh;
+                }
             }
             // v of this thread's row, loaded while the accumulators finish
             float vreg[kSeg];
@@ -1002,13 +1017,33 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 float *orow = a.o + (int64_t(n0) * a.Hv + h) * D + row;
                 float *urow = a.replay + (int64_t(n0) * a.Hv + h) * a.rstride + D + row;
                 const int64_t ostep = int64_t(a.Hv) * D, ustep = int64_t(a.Hv) * a.rstride;
+                if (full) {
 #pragma unroll
-                for (int t = 0; t < kSeg; ++t) {
-                    if (t < lc) {
+                    for (int t = 0; t < kSeg; ++t) {
                         const float2 o01 = gdn::f2unpack(op[t / 2]), u01 = gdn::f2unpack(up[t / 2]);
-                        orow[t * ostep] = (t & 1) ? o01.y : o01.x;
-                        urow[t * ustep] = (t & 1) ? u01.y : u01.x;
+                        stg_o[t * D + row] = (t & 1) ? o01.y : o01.x;
+                        stg_u[t * D + row] = (t & 1) ? u01.y : u01.x;
                     }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < kSeg; ++t) {
+                        if (t < lc) {
+                            const float2 o01 = gdn::f2unpack(op[t / 2]), u01 = gdn::f2unpack(up[t / 2]);
+                            orow[t * ostep] = (t & 1) ? o01.y : o01.x;
+                            urow[t * ustep] = (t & 1) ? u01.y : u01.x;
+                        }
+                    }
+                }
+            }
+            // a full item's o, k^ and u tiles leave by three TMA stores
+            if (full) {
+                gdn::fence_proxy_async_smem();
+                team_sync(team);
+                if (ttid == 0 && staged) {
+                    gdn::tma_store_3d(&omap, stg_o, 0, h, n0);
+                    gdn::tma_store_3d(&rmap, stg_k, 0, h, n0);
+                    gdn::tma_store_3d(&rmap, stg_u, D, h, n0);
+                    gdn::bulk_commit_group();
                 }
             }
             // the lo rows of the next item's B (its q/k rows were requested when
@@ -1017,6 +1052,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             // after a timeout the team keeps looping (every wait now returns at
             // once) so that all four warps meet at each team barrier
         }
+        if (ttid == 0) gdn::bulk_wait0();  // the last output stores are complete
         // after a timeout, a q/k copy may still be in flight: wait for it (bounded)
         if (*abort_flag && qk_issued > 0)
             gdn::mbar_wait_bounded(bars + B_QFULL + team, uint32_t((qk_issued - 1) & 1));
@@ -1097,9 +1133,26 @@ int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C, uint3
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
 }
 
+// An output tensor [N][H_v][row_floats] (o, or the replay rows) for TMA stores
+// of [16 nodes][1 head][d floats] tiles, unswizzled.
+int encode_out_map(CUtensorMap *map, float *base, int64_t N, int64_t Hv, int64_t row_floats, int D) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return GDN_ERR_TMA;
+    cuuint64_t gdim[3] = {cuuint64_t(row_floats), cuuint64_t(Hv), cuuint64_t(N)};
+    cuuint64_t gstride[2] = {cuuint64_t(row_floats) * 4, cuuint64_t(Hv * row_floats) * 4};
+    cuuint32_t box[3] = {cuuint32_t(D), 1, 16};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
+}
+
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
-    CUtensorMap xmap;
+    CUtensorMap xmap, omap, rmap;
     if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C, 16, 32, true)) return rc;
+    if (int rc = encode_out_map(&omap, a.o, a.N, a.Hv, wsv::D, wsv::D)) return rc;
+    if (int rc = encode_out_map(&rmap, a.replay, a.N, a.Hv, a.rstride, wsv::D)) return rc;
     auto k = tree_verify_ws_kernel;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(wsv::BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
@@ -1108,7 +1161,7 @@ int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
     if (sms <= 0) return GDN_ERR_LAUNCH;
     // one CTA per SM, each with at most kMaxItems items (more CTAs queue behind)
     int64_t grid = std::max<int64_t>(std::min<int64_t>(items, sms), (items + wsv::kMaxItems - 1) / wsv::kMaxItems);
-    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, a) == cudaSuccess
+    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, omap, rmap, a) == cudaSuccess
                ? GDN_OK
                : GDN_ERR_LAUNCH;
 }
