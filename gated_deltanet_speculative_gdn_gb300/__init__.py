@@ -32,7 +32,7 @@ GDN_DEV_BAD_WINDOW = 7
 
 EXPORTED_SYMBOLS = ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit",
                     "gdn_conv_tree_step_compact", "gdn_commit_compact", "gdn_gated_rmsnorm",
-                    "gdn_decode_step",
+                    "gdn_decode_step", "gdn_test_stall_next_verify",
                     "gdn_status_str", "gdn_replay_row_floats")
 
 if not os.path.exists(LIB_PATH):
@@ -73,6 +73,8 @@ lib.gdn_commit.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P]
 lib.gdn_conv_tree_step_compact.argtypes = [_DP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 lib.gdn_commit_compact.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _P]
 lib.gdn_gated_rmsnorm.argtypes = [_DP, _P, _P, _I64, _P, ctypes.c_float, ctypes.c_int, _P, _P]
+lib.gdn_test_stall_next_verify.argtypes = [ctypes.c_uint64]
+lib.gdn_test_stall_next_verify.restype = None
 lib.gdn_decode_step.argtypes = [_DP, _P, _I64, _P, _P, _P, _I64, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
                                 _P]
 for _f in ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit", "gdn_conv_tree_step_compact",
@@ -176,3 +178,7 @@ def gdn_decode_step(dims: GdnDims, x, x_stride: int, conv_w, conv_hist, ba, ba_s
                              int(ba_stride), _ptr(dt_bias), _ptr(A), _ptr(ssm), float(q_scale), _ptr(slot_map),
                              _ptr(xc), _ptr(o), _ptr(status), _stream(stream))
     return _check("gdn_decode_step", rc, raise_on_error)
+
+
+def gdn_test_stall_next_verify(wait_ns: int) -> None:
+    lib.gdn_test_stall_next_verify(int(wait_ns))

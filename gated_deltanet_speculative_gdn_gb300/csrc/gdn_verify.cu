@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
@@ -86,6 +87,7 @@ struct VerifyArgs {
     int64_t rstride;
     int32_t *status;
     int S, N, P, Hk, Hv, C, max_nodes;
+    uint64_t stall_ns;  // test hook: a wait that nothing ends, for this long (0: none)
 };
 
 // Row `row`, float4 column group `kc` of the TMA-staged state.  For d >= 32 the
@@ -504,7 +506,8 @@ constexpr int B_GFULL = B_BREADY + 2;      // per team: Gram terms complete (1)
 constexpr int B_ACCFULL = B_GFULL + 2;     // per team: accumulators complete (1 from each product issuer)
 constexpr int B_ACCEMPTY = B_ACCFULL + 2;  // per team: accumulators read (128)
 constexpr int B_DRAIN = B_ACCEMPTY + 2;    // the issuers' last tensor-core work done (1 from each)
-constexpr int N_BARS = B_DRAIN + 1;
+constexpr int B_NEVER = B_DRAIN + 1;       // nothing arrives: the timeout test's wait
+constexpr int N_BARS = B_NEVER + 1;
 constexpr int W_BARS = 2 * T_WORDS;
 constexpr int W_TMEM = W_BARS + 2 * N_BARS;
 constexpr int W_ABORT = W_TMEM + 1;
@@ -808,6 +811,11 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             return true;
         };
         bool staged_nx = split_b(team);
+        // test hook: team 0 of CTA 0 waits on a barrier that nothing completes,
+        // so the wait runs out, and every role drains and leaves
+        if (a.stall_ns && blockIdx.x == 0 && team == 0 &&
+            !gdn::mbar_wait_bounded(bars + B_NEVER, 0, a.stall_ns))
+            *abort_flag = 1;
 
         for (int v = team; v < nv; v += 2) {
             const int ut = v >> 1;
@@ -1148,7 +1156,11 @@ int encode_out_map(CUtensorMap *map, float *base, int64_t N, int64_t Hv, int64_t
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
 }
 
-int launch_tc(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
+std::atomic<uint64_t> g_stall_ns{0};
+
+int launch_tc(const CUtensorMap &map, const VerifyArgs &a_in, cudaStream_t st) {
+    VerifyArgs a = a_in;
+    a.stall_ns = g_stall_ns.exchange(0);
     CUtensorMap xmap, omap, rmap;
     if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C, 16, 32, true)) return rc;
     if (int rc = encode_out_map(&omap, a.o, a.N, a.Hv, wsv::D, wsv::D)) return rc;
@@ -1211,7 +1223,7 @@ extern "C" int gdn_tree_verify(const gdn_dims *dims, const float *xc, const floa
     CUtensorMap map;
     if ((rc = encode_state_map(&map, ssm, P, Hv, int(D)))) return rc;
     VerifyArgs a{xc, ba, ba_stride, dt_bias, A, q_scale, parents, node_off, slot_map, o, replay, replay_stride,
-                 status, int(S), int(N), int(P), dims->h_k, int(Hv), int(C), dims->max_seq_nodes};
+                 status, int(S), int(N), int(P), dims->h_k, int(Hv), int(C), dims->max_seq_nodes, 0};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (D) {
         case 16: return launch_d<16>(map, a, st);
@@ -1219,4 +1231,8 @@ extern "C" int gdn_tree_verify(const gdn_dims *dims, const float *xc, const floa
         case 64: return launch_d<64>(map, a, st);
         default: return launch_d<128>(map, a, st);
     }
+}
+
+extern "C" void gdn_test_stall_next_verify(uint64_t wait_ns) {
+    g_stall_ns.store(std::min<uint64_t>(wait_ns, gdn::kWaitLimitNs));
 }

@@ -54,7 +54,15 @@
  *   floor(h / G).
  * Streams.  All work is enqueued on `stream` (a cudaStream_t; NULL = the
  *   legacy default stream) and is asynchronous.  verify -> (host decides
- *   acceptance) -> commit must be ordered by the caller's stream.
+ *   acceptance) -> commit must be ordered by the caller's stream.  The
+ *   library's kernels use programmatic dependent launch: each may start
+ *   while the previous kernel on the stream finishes, and waits for it to
+ *   complete before touching any buffer the library writes.  They may read
+ *   the pure inputs (parents, node_off, slot_map, accepted, win_ref) before
+ *   that wait, so a caller that produces those in a kernel on the same stream
+ *   must not let that kernel trigger its dependents early
+ *   (cudaTriggerProgrammaticLaunchCompletion / griddepcontrol.launch_dependents
+ *   before its writes); a plain launch, or a copy, is always safe.
  * Access.  gdn_conv_tree_step and gdn_tree_verify never write the pools
  *   (`conv_hist`, `ssm`).  Only gdn_commit writes them.  No float atomics:
  *   results are bit-for-bit reproducible run to run.
@@ -247,6 +255,16 @@ int gdn_decode_step(const gdn_dims *dims, const float *x, int64_t x_stride, cons
                     float *conv_hist, const float *ba, int64_t ba_stride, const float *dt_bias,
                     const float *A, float *ssm, float q_scale, const int32_t *slot_map, float *xc,
                     float *o, int32_t *status, void *stream);
+
+/* Test hook for the device timeout path.  The next gdn_tree_verify call that
+ * runs the tensor-core kernel (d = 128, max_seq_nodes <= 16) makes one team of
+ * its first CTA wait on a barrier that nothing ever completes, for wait_ns
+ * (capped at the library's 2 s wait limit); the wait runs out, every role of
+ * that CTA drains its copies and tensor-core work and leaves, and the call
+ * reports GDN_DEV_TIMEOUT in *status (its outputs are then unspecified).  The
+ * hook is consumed by that one call.  The paper has no counterpart; it exists
+ * so that the bounded-wait path can be tested without a GPU fault. */
+void gdn_test_stall_next_verify(uint64_t wait_ns);
 
 /* Name of a host or device status code ("GDN_OK", "GDN_DEV_DUP_SLOT", ...);
  * "unknown" for any other value.  Never NULL. */

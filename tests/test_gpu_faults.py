@@ -97,3 +97,19 @@ def test_commit_refuses_after_an_earlier_error():
     torch.cuda.synchronize()
     assert int(status.item()) == 99
     assert_pools_unchanged(pools, lp)
+
+
+def test_verify_wait_that_runs_out_reports_timeout_and_the_context_survives():
+    """A test hook makes one team of the first CTA of the tensor-core verify
+    wait on a barrier that nothing completes; the wait runs out (20 ms), every
+    role drains and leaves, *status reads GDN_DEV_TIMEOUT and the commit that
+    follows writes nothing.  The next call on the same context is exact."""
+    from gpu_harness import compare, run_oracle
+    b, lp = custom_batch(18, 2, 4, 128, [16, 9, 12], max_nodes=16)
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    G.gdn_test_stall_next_verify(20_000_000)
+    g = run_gpu(b, pools)
+    assert g.status == G.GDN_DEV_TIMEOUT, G.gdn_status_str(g.status)
+    assert_pools_unchanged(pools, lp)
+    g2 = run_gpu(b, pools)
+    compare(g2, run_oracle(b, lp.ssm, lp.conv_hist))
