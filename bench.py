@@ -211,6 +211,9 @@ class DeviceWorkload:
         import gated_deltanet_speculative_gdn_gb300 as G
         self.G = G
         self.dims = G.GdnDims.make(sh.n_seqs, N, sh.n_slots, sh.h_k, sh.h_v, sh.d, sp.max_seq_nodes)
+        # chain workloads go through the chain entry point (chunked form, d = 128)
+        self.chain = sp.tree_kind == "chain" and sh.d == 128
+        self.verify = G.gdn_chain_verify if self.chain else G.gdn_tree_verify
 
     def step(self, r, events=None, inputs=None):
         """conv -> verify -> commit on round r; events[i] recorded before call i."""
@@ -226,9 +229,8 @@ class DeviceWorkload:
                                  self.slot_map, self.xc, self.win, self.status)
         if events:
             events[1].record()
-        G.gdn_tree_verify(self.dims, self.xc, R["ba"], 2 * sh.h_v, self.dt, self.A, self.ssm, 1.0,
-                          R["parents"], R["node_off"], self.slot_map, self.o, self.replay, self.rs,
-                          self.status)
+        self.verify(self.dims, self.xc, R["ba"], 2 * sh.h_v, self.dt, self.A, self.ssm, 1.0,
+                    R["parents"], R["node_off"], self.slot_map, self.o, self.replay, self.rs, self.status)
         if events:
             events[2].record()
         if self.compact:
@@ -672,7 +674,8 @@ def main():
         sweep[v] = {"nodes_per_s": round(r["wl"].N / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
                     "step_gbs": round(b / (ms * 1e-3) / 1e9, 1),
                     "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
-                    "kernels_ms": {k: round(statistics.mean(x), 5) for k, x in r["per"].items()}}
+                    "kernels_ms": {k: round(statistics.mean(x), 5) for k, x in r["per"].items()},
+                    "verify_entry": r["wl"].verify.__name__}
 
     cpu = None
     spot = None

@@ -30,7 +30,7 @@ GDN_DEV_BAD_NODE_OFF, GDN_DEV_BAD_PARENT, GDN_DEV_BAD_SLOT = 1, 2, 3
 GDN_DEV_DUP_SLOT, GDN_DEV_BAD_ACCEPTED, GDN_DEV_TIMEOUT = 4, 5, 6
 GDN_DEV_BAD_WINDOW = 7
 
-EXPORTED_SYMBOLS = ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit",
+EXPORTED_SYMBOLS = ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_chain_verify", "gdn_commit",
                     "gdn_conv_tree_step_compact", "gdn_commit_compact", "gdn_gated_rmsnorm",
                     "gdn_decode_step", "gdn_test_stall_next_verify",
                     "gdn_status_str", "gdn_replay_row_floats")
@@ -69,6 +69,7 @@ _DP = ctypes.POINTER(GdnDims)
 lib.gdn_conv_tree_step.argtypes = [_DP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 lib.gdn_tree_verify.argtypes = [_DP, _P, _P, _I64, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                                 _P, _P, _I64, _P, _P]
+lib.gdn_chain_verify.argtypes = lib.gdn_tree_verify.argtypes
 lib.gdn_commit.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P]
 lib.gdn_conv_tree_step_compact.argtypes = [_DP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 lib.gdn_commit_compact.argtypes = [_DP, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _P]
@@ -77,7 +78,7 @@ lib.gdn_test_stall_next_verify.argtypes = [ctypes.c_uint64]
 lib.gdn_test_stall_next_verify.restype = None
 lib.gdn_decode_step.argtypes = [_DP, _P, _I64, _P, _P, _P, _I64, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
                                 _P]
-for _f in ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_commit", "gdn_conv_tree_step_compact",
+for _f in ("gdn_conv_tree_step", "gdn_tree_verify", "gdn_chain_verify", "gdn_commit", "gdn_conv_tree_step_compact",
            "gdn_commit_compact", "gdn_gated_rmsnorm", "gdn_decode_step"):
     getattr(lib, _f).restype = ctypes.c_int
 lib.gdn_status_str.argtypes = [ctypes.c_int]
@@ -138,6 +139,16 @@ def gdn_tree_verify(dims: GdnDims, xc, ba, ba_stride: int, dt_bias, A, ssm, q_sc
                              _ptr(slot_map), _ptr(o), _ptr(replay), int(replay_stride),
                              _ptr(status), _stream(stream))
     return _check("gdn_tree_verify", rc, raise_on_error)
+
+
+def gdn_chain_verify(dims: GdnDims, xc, ba, ba_stride: int, dt_bias, A, ssm, q_scale: float,
+                     parents, node_off, slot_map, o, replay, replay_stride: int, status,
+                     stream=None, raise_on_error: bool = True) -> int:
+    rc = lib.gdn_chain_verify(ctypes.byref(dims), _ptr(xc), _ptr(ba), int(ba_stride), _ptr(dt_bias),
+                              _ptr(A), _ptr(ssm), float(q_scale), _ptr(parents), _ptr(node_off),
+                              _ptr(slot_map), _ptr(o), _ptr(replay), int(replay_stride),
+                              _ptr(status), _stream(stream))
+    return _check("gdn_chain_verify", rc, raise_on_error)
 
 
 def gdn_commit(dims: GdnDims, accepted, parents, node_off, slot_map, replay, replay_stride: int,

@@ -10,6 +10,8 @@
  *                       q/k L2 norm computed in the kernel; reads the
  *                       recurrent state read-only from its slot and emits the
  *                       attention output and one replay row per node and head.
+ *   gdn_chain_verify    the same verify for batches of chains (node i's parent
+ *                       is node i - 1), in chunked form.
  *   gdn_commit          once acceptance is known, advances the persistent conv
  *                       and recurrent state of every sequence by its accepted
  *                       root-to-node path, on the device, as one transaction.
@@ -170,6 +172,25 @@ int gdn_tree_verify(const gdn_dims *dims, const float *xc, const float *ba,
                     const int32_t *node_off, const int32_t *slot_map, float *o,
                     float *replay, int64_t replay_stride, int32_t *status,
                     void *stream);
+
+/* Chain verify (lucebox PR #707, Scope and fallback: dense chains keep a path
+ * of their own; TensorSharp PR #175, change 1: a run of tokens goes through a
+ * chunked GDN kernel).  The same operation, arguments, outputs and replay rows
+ * as gdn_tree_verify, for batches in which every sequence's nodes form a chain
+ * (parents[node_off[s] + i] = i - 1), d = 128 only.  It evaluates the chain in
+ * chunks of 16 nodes and carries the state on chip between them, so long
+ * chains (up to max_seq_nodes = 64) cost little more per node than short ones.
+ * The replay rows feed gdn_commit / gdn_commit_compact unchanged.
+ * Host errors: as gdn_tree_verify, and GDN_ERR_DIMS when d != 128.
+ * Device errors: GDN_DEV_BAD_NODE_OFF, GDN_DEV_BAD_SLOT, GDN_DEV_BAD_PARENT
+ * (a sequence that is not a chain; its outputs are not written),
+ * GDN_DEV_TIMEOUT. */
+int gdn_chain_verify(const gdn_dims *dims, const float *xc, const float *ba,
+                     int64_t ba_stride, const float *dt_bias, const float *A,
+                     const float *ssm, float q_scale, const int32_t *parents,
+                     const int32_t *node_off, const int32_t *slot_map, float *o,
+                     float *replay, int64_t replay_stride, int32_t *status,
+                     void *stream);
 
 /* Replay-log commit (lucebox PR #707, Summary; TensorSharp PR #175 on-device
  * commit; lucebox PR #659 transaction preflight and stream ordering).

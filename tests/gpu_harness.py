@@ -103,9 +103,11 @@ class GpuOut:
 
 def run_gpu(b: Batch, pools: GpuPools, q_scale: float = 1.0, commit: bool = True,
             x_pad: int = 0, ba_pad: int = 0, replay_pad: int = 0,
-            xc_override: Optional[np.ndarray] = None, compact: bool = False) -> GpuOut:
+            xc_override: Optional[np.ndarray] = None, compact: bool = False,
+            chain: bool = False) -> GpuOut:
     """conv -> verify -> commit on the device (pools updated in place); with
-    compact=True the windows travel as references (the compact entry points)."""
+    compact=True the windows travel as references (the compact entry points),
+    with chain=True verify goes through gdn_chain_verify."""
     C, N, Hv, d = b.C, b.N, b.Hv, b.d
     dm = b.gdims()
     xs = C + x_pad
@@ -131,7 +133,8 @@ def run_gpu(b: Batch, pools: GpuPools, q_scale: float = 1.0, commit: bool = True
     else:
         G.gdn_conv_tree_step(dm, x, xs, w, pools.conv_hist, par, off, sm, xc, win, status)
     xin = xc if xc_override is None else dev(xc_override.astype(np.float32))
-    G.gdn_tree_verify(dm, xin, ba, bas, dt, A, pools.ssm, q_scale, par, off, sm, o, rep, rs, status)
+    verify = G.gdn_chain_verify if chain else G.gdn_tree_verify
+    verify(dm, xin, ba, bas, dt, A, pools.ssm, q_scale, par, off, sm, o, rep, rs, status)
     if commit and compact:
         G.gdn_commit_compact(dm, acc, par, off, sm, rep, rs, x, xs, wref, pools.ssm, pools.conv_hist, status)
     elif commit:

@@ -74,6 +74,17 @@ def verify(d, **kw):
                              stream=0, raise_on_error=False)
 
 
+def chain_verify(d, **kw):
+    args = dict(xc=FAKE, ba=FAKE * 2, ba_stride=2 * d.h_v, dt_bias=FAKE * 3, A=FAKE * 4, ssm=FAKE * 5,
+                parents=FAKE * 6, node_off=FAKE * 7, slot_map=FAKE * 8, o=FAKE * 9, replay=FAKE * 10,
+                replay_stride=G.gdn_replay_row_floats(d.d_k, d.d_v), status=FAKE * 11)
+    args.update(kw)
+    return G.gdn_chain_verify(d, args["xc"], args["ba"], args["ba_stride"], args["dt_bias"], args["A"],
+                              args["ssm"], 1.0, args["parents"], args["node_off"], args["slot_map"],
+                              args["o"], args["replay"], args["replay_stride"], args["status"],
+                              stream=0, raise_on_error=False)
+
+
 def commit(d, **kw):
     args = dict(accepted=FAKE, parents=FAKE * 2, node_off=FAKE * 3, slot_map=FAKE * 4, replay=FAKE * 5,
                 replay_stride=G.gdn_replay_row_floats(d.d_k, d.d_v), win=FAKE * 6, ssm=FAKE * 7,
@@ -182,3 +193,22 @@ def test_compact_host_validation():
                                 FAKE * 8, FAKE * 9, FAKE * 10, stream=0, raise_on_error=False) == G.GDN_ERR_STRIDE
     assert G.gdn_commit_compact(d, FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, rs, FAKE * 6, C, None,
                                 FAKE * 8, FAKE * 9, FAKE * 10, stream=0, raise_on_error=False) == G.GDN_ERR_NULL
+
+
+def test_chain_verify_host_validation():
+    """The chain verify takes gdn_tree_verify's arguments and checks them the
+    same way; it serves d = 128 only."""
+    for d in (16, 32, 64):
+        assert chain_verify(dims(d=d)) == G.GDN_ERR_DIMS
+    for bad in (dict(max_seq_nodes=65), dict(h_k=3, h_v=4), dict(n_slots=0)):
+        assert chain_verify(dims(d=128, **bad)) == G.GDN_ERR_DIMS
+    d = dims(d=128)
+    assert chain_verify(d, ssm=None) == G.GDN_ERR_NULL
+    assert chain_verify(d, status=None) == G.GDN_ERR_NULL
+    assert chain_verify(d, ba_stride=2 * d.h_v - 1) == G.GDN_ERR_STRIDE
+    assert chain_verify(d, replay_stride=2 * 128) == G.GDN_ERR_STRIDE
+    assert chain_verify(d, replay_stride=2 * 128 + 2) == G.GDN_ERR_STRIDE
+    assert chain_verify(d, ssm=FAKE * 5 + 8) == G.GDN_ERR_ALIGN
+    assert chain_verify(d, o=FAKE * 5 + 64) == G.GDN_ERR_ALIAS
+    assert chain_verify(dims(d=128, n_nodes=0)) == G.GDN_OK
+    assert chain_verify(dims(d=128, n_seqs=0, n_nodes=0), xc=None) == G.GDN_OK
