@@ -211,8 +211,9 @@ class DeviceWorkload:
         import gated_deltanet_speculative_gdn_gb300 as G
         self.G = G
         self.dims = G.GdnDims.make(sh.n_seqs, N, sh.n_slots, sh.h_k, sh.h_v, sh.d, sp.max_seq_nodes)
-        # chain workloads go through the chain entry point (chunked form, d = 128)
-        self.chain = sp.tree_kind == "chain" and sh.d == 128
+        # chains longer than one 16-node chunk go through the chain entry point
+        # (chunked form, d = 128); shorter ones are single tensor-core items
+        self.chain = sp.tree_kind == "chain" and sh.d == 128 and sp.max_seq_nodes > 16
         self.verify = G.gdn_chain_verify if self.chain else G.gdn_tree_verify
 
     def step(self, r, events=None, inputs=None):

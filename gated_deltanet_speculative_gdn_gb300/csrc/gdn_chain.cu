@@ -49,6 +49,10 @@ constexpr int KQS = 8 * 20 + 4;  // padded k^/q^ row: eight groups of 16 floats 
 constexpr int RS = 36;       // row stride of the a_t | b_t tile [state row][32]
 constexpr int US = 20;       // row stride of the u tile [state row][node]
 constexpr int CS = 20;       // row stride of the 16 x 16 coefficient matrices
+// Column slot of node t in the transposed matrices: even nodes first, then odd
+// ones, so that the two threads of a state row (one per parity) each read
+// their eight entries of a column as two float4.
+__host__ __device__ constexpr int tslot(int t) { return (t & 1) * 8 + (t >> 1); }
 // what an item's sequence asks for: run, skip (empty), or a GDN_DEV_* code (> 0)
 constexpr int kRun = -1, kSkip = 0;
 
@@ -60,8 +64,9 @@ constexpr int KQH = VB + 2 * kChunk * D;     // [32][KQS] k^ (0..15) | q^ (16..3
 constexpr int RES = KQH + 2 * kChunk * KQS;  // [128][RS] a_t (0..15) | b_t (16..31)
 constexpr int UB = RES + D * RS;             // [128][US] u_t per state row
 constexpr int CKM = UB + D * US;             // [16][CS] gamma_{j->t} k^_j.k^_t (j < t)
-constexpr int CQM = CKM + kChunk * CS;       // [16][CS] gamma_{j->t} k^_j.q^_t (j <= t)
-constexpr int BETA = CQM + kChunk * CS;      // [16]
+constexpr int CQT = CKM + kChunk * CS;       // [16 j][CS] gamma_{j->t} k^_j.q^_t (j <= t), at tslot(t)
+constexpr int TT = CQT + kChunk * CS;        // [16 j][CS] T[t][j], at tslot(t)
+constexpr int BETA = TT + kChunk * CS;       // [16]
 constexpr int DEC = BETA + kChunk;           // [16]
 constexpr int GAM = DEC + kChunk;            // [16] Gamma_t
 constexpr int WEND = GAM + kChunk;           // [16] gamma_{j->L-1}
@@ -129,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 2) chain_verify_kernel(const ChainAr
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = tid >> 3, cg = tid & 7;  // contraction / update: rows 4rg .. 4rg+3, columns 16cg ..
-    const int si = tid >> 1, sh = tid & 1;  // solve: state row si; outputs for nodes 8sh .. 8sh+7
     gdn::grid_dep_launch();
     if (tid == 0) {
         gdn::mbar_init(bkq, 1);
@@ -341,7 +345,10 @@ __global__ void __launch_bounds__(kThreads, 2) chain_verify_kernel(const ChainAr
                         for (int s2 = j + 1; s2 <= t; ++s2) g *= sm[DEC + s2];
                         coef = g * acc[e];
                     }
-                    sm[(kk ? CKM : CQM) + t * CS + j] = coef;
+                    if (kk)
+                        sm[CKM + t * CS + j] = coef;
+                    else
+                        sm[CQT + j * CS + tslot(t)] = coef;
                 }
                 if (tid < kChunk) {
                     float gam = 1.f;
@@ -356,6 +363,23 @@ __global__ void __launch_bounds__(kThreads, 2) chain_verify_kernel(const ChainAr
                 }
             }
             __syncthreads();
+
+            // ---- T = (I + diag(beta) CK)^-1 diag(beta), one column per lane of warp
+            //      0 (forward substitution down the column, kept in registers) -----
+            if (warp == 0 && lane < kChunk) {
+                const int j = lane;
+                float tc[kChunk];
+#pragma unroll
+                for (int t = 0; t < kChunk; ++t) {
+                    const float *ck = sm + CKM + t * CS;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < t; ++s2) acc = fmaf(ck[s2], tc[s2], acc);  // tc[s2] = 0 for s2 < j
+                    const float b = sm[BETA + t];
+                    tc[t] = t == j ? b : (t > j ? -b * acc : 0.f);
+                    sm[TT + j * CS + tslot(t)] = tc[t];
+                }
+            }
 
             // ---- C: a_t = S k^_t, b_t = S q^_t for the four rows of each thread --
             {
@@ -399,64 +423,66 @@ __global__ void __launch_bounds__(kThreads, 2) chain_verify_kernel(const ChainAr
                     if ((cg & 1) == (v & 1)) res[(4 * rg + (cg >> 1)) * RS + v] = p[0];
                 }
             }
-            // the rows a thread pair solves were reduced inside its own warp
-            __syncwarp();
-
-            // ---- D: u by forward substitution along the chunk, then o -------------
+            // ---- D: u = T e (e_j = v_j - Gamma_j a_j), then o = Gamma b + CQ u; the
+            //      two threads of state row si take the even and the odd nodes ------
+            __syncthreads();  // T and every a_t / b_t are in place
             {
+                const int si = tid >> 1, sh = tid & 1;
                 uint64_t *bv = bvv + vb;
                 if (!gdn::mbar_wait_bounded(bv, vb ? ph_v1 : ph_v0)) timed_out = true;
-                (vb ? ph_v1 : ph_v0) ^= 1;
-                (vb ? pend_v1 : pend_v0) = false;
                 const float *vrow = sm + VB + vb * kChunk * D + si;
                 const float *rrow = sm + RES + si * RS;
-                float u[kChunk];
+                float u[8];
 #pragma unroll
-                for (int t = 0; t < kChunk; ++t) {
-                    // S' k^_t = Gamma_t a_t + sum_{j<t} CK[t][j] u_j
-                    float sk = sm[GAM + t] * rrow[t];
-                    const float *ck = sm + CKM + t * CS;
-#pragma unroll
-                    for (int j4 = 0; j4 < (t + 3) / 4; ++j4) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(ck + 4 * j4);
-                        if (4 * j4 + 0 < t) sk = fmaf(cv.x, u[4 * j4 + 0], sk);
-                        if (4 * j4 + 1 < t) sk = fmaf(cv.y, u[4 * j4 + 1], sk);
-                        if (4 * j4 + 2 < t) sk = fmaf(cv.z, u[4 * j4 + 2], sk);
-                        if (4 * j4 + 3 < t) sk = fmaf(cv.w, u[4 * j4 + 3], sk);
-                    }
-                    u[t] = t < L ? sm[BETA + t] * (vrow[t * D] - sk) : 0.f;
+                for (int k = 0; k < 8; ++k) u[k] = 0.f;
+#pragma unroll 4
+                for (int j = 0; j < L; ++j) {
+                    const float e = vrow[j * D] - sm[GAM + j] * rrow[j];
+                    const float4 t0 = *reinterpret_cast<const float4 *>(sm + TT + j * CS + 8 * sh);
+                    const float4 t1 = *reinterpret_cast<const float4 *>(sm + TT + j * CS + 8 * sh + 4);
+                    u[0] = fmaf(t0.x, e, u[0]);
+                    u[1] = fmaf(t0.y, e, u[1]);
+                    u[2] = fmaf(t0.z, e, u[2]);
+                    u[3] = fmaf(t0.w, e, u[3]);
+                    u[4] = fmaf(t1.x, e, u[4]);
+                    u[5] = fmaf(t1.y, e, u[5]);
+                    u[6] = fmaf(t1.z, e, u[6]);
+                    u[7] = fmaf(t1.w, e, u[7]);
                 }
                 float *urow = sm + UB + si * US;
-                if (sh == 0) {
-                    *reinterpret_cast<float4 *>(urow) = make_float4(u[0], u[1], u[2], u[3]);
-                    *reinterpret_cast<float4 *>(urow + 4) = make_float4(u[4], u[5], u[6], u[7]);
-                } else {
-                    *reinterpret_cast<float4 *>(urow + 8) = make_float4(u[8], u[9], u[10], u[11]);
-                    *reinterpret_cast<float4 *>(urow + 12) = make_float4(u[12], u[13], u[14], u[15]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int t = 2 * k + sh;
+                    urow[t] = u[k];
+                    if (t < L) a.replay[((nf + t) * a.Hv + h) * a.rstride + D + si] = u[k];
+                }
+                __syncwarp();
+                float ov[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) ov[k] = sm[GAM + 2 * k + sh] * rrow[kChunk + 2 * k + sh];
+#pragma unroll 4
+                for (int j = 0; j < L; ++j) {
+                    const float uj = urow[j];
+                    const float4 c0 = *reinterpret_cast<const float4 *>(sm + CQT + j * CS + 8 * sh);
+                    const float4 c1 = *reinterpret_cast<const float4 *>(sm + CQT + j * CS + 8 * sh + 4);
+                    ov[0] = fmaf(c0.x, uj, ov[0]);
+                    ov[1] = fmaf(c0.y, uj, ov[1]);
+                    ov[2] = fmaf(c0.z, uj, ov[2]);
+                    ov[3] = fmaf(c0.w, uj, ov[3]);
+                    ov[4] = fmaf(c1.x, uj, ov[4]);
+                    ov[5] = fmaf(c1.y, uj, ov[5]);
+                    ov[6] = fmaf(c1.z, uj, ov[6]);
+                    ov[7] = fmaf(c1.w, uj, ov[7]);
                 }
 #pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    const int t = 8 * sh + tt;
-                    if (t < L) a.replay[((nf + t) * a.Hv + h) * a.rstride + D + si] = sh ? u[8 + tt] : u[tt];
-                }
-#pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    const int t = 8 * sh + tt;
-                    // o_t = Gamma_t b_t + sum_{j<=t} CQ[t][j] u_j
-                    float oq = sm[GAM + t] * rrow[kChunk + t];
-                    const float *cqr = sm + CQM + t * CS;
-#pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(cqr + 4 * j4);
-                        oq = fmaf(cv.x, u[4 * j4 + 0], oq);
-                        oq = fmaf(cv.y, u[4 * j4 + 1], oq);
-                        oq = fmaf(cv.z, u[4 * j4 + 2], oq);
-                        oq = fmaf(cv.w, u[4 * j4 + 3], oq);
-                    }
-                    if (t < L) a.o[((nf + t) * a.Hv + h) * D + si] = a.q_scale * oq;
+                for (int k = 0; k < 8; ++k) {
+                    const int t = 2 * k + sh;
+                    if (t < L) a.o[((nf + t) * a.Hv + h) * D + si] = a.q_scale * ov[k];
                 }
             }
-            __syncwarp();
+            (vb ? ph_v1 : ph_v0) ^= 1;
+            (vb ? pend_v1 : pend_v0) = false;
+            __syncthreads();  // every u_t is in place
 
             // ---- E: the state at the end of the chunk -----------------------------
             if (c + 1 < nchunks) {
