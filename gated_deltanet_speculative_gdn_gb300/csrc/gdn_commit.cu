@@ -48,10 +48,11 @@ struct CommitArgs {
 
 __global__ void __launch_bounds__(256) commit_preflight_kernel(const CommitArgs a) {
     gdn::grid_dep_launch();
-    gdn::grid_dep_wait();  // status
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= a.S) return;
+    // the checks that need only the caller's index inputs run before the wait,
+    // while the verify launched before this kernel finishes
     const int n0 = a.node_off[s], n1 = a.node_off[s + 1];
     const int acc = a.accepted[s], slot = a.slot_map[s];
     int err = 0;
@@ -76,12 +77,13 @@ __global__ void __launch_bounds__(256) commit_preflight_kernel(const CommitArgs 
             for (int s2 = lane; s2 < a.S; s2 += 32)
                 dup |= (s2 != s && a.accepted[s2] >= 0 && a.slot_map[s2] == slot);
             if (!err && __any_sync(0xffffffffu, dup)) err = GDN_DEV_DUP_SLOT;
-            if (!err && a.wref) {
-                for (int j = 0; j < 3; ++j) {
-                    const int r = a.wref[(int64_t(n0) + acc) * 3 + j];
-                    if (r < -3 || r >= a.N) err = GDN_DEV_BAD_WINDOW;
-                }
-            }
+        }
+    }
+    gdn::grid_dep_wait();  // status; the compact form's window references come from the conv
+    if (!err && acc >= 0 && a.wref) {
+        for (int j = 0; j < 3; ++j) {
+            const int r = a.wref[(int64_t(n0) + acc) * 3 + j];
+            if (r < -3 || r >= a.N) err = GDN_DEV_BAD_WINDOW;
         }
     }
     if (err && lane == 0) gdn::record_status(a.status, err);

@@ -512,7 +512,8 @@ constexpr int W_BARS = 2 * T_WORDS;
 constexpr int W_TMEM = W_BARS + 2 * N_BARS;
 constexpr int W_ABORT = W_TMEM + 1;
 constexpr int W_NV = W_ABORT + 1;
-constexpr int W_LIST = (W_NV + 4) & ~3;            // kMaxItems x int4 (item, n0, ns, slot), 16-B aligned
+constexpr int W_ERR = W_NV + 1;                    // an index error found during set-up
+constexpr int W_LIST = (W_ERR + 4) & ~3;           // kMaxItems x int4 (item, n0, ns, slot), 16-B aligned
 constexpr int SMALL_WORDS = W_LIST + 4 * kMaxItems;
 constexpr size_t BYTES = SMALL + SMALL_WORDS * 4 + 1024;
 static_assert(BYTES <= 227 * 1024, "shared memory");
@@ -572,10 +573,14 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int total = a.S * a.Hv;
     gdn::grid_dep_launch();
-    gdn::grid_dep_wait();  // xc, the state pool, status
 
-    // ---- set-up: this CTA's valid items, barriers, tensor memory -------------
+    // ---- set-up: this CTA's valid items, barriers, tensor memory.  It reads
+    //      only the caller's index inputs, so it runs before the wait for the
+    //      previous kernel; so do L2 requests for the first items' states (a
+    //      hint: whatever writes them later still lands in L2). --------------
     if (warp == 0) {
+        if (lane == 0) words[W_ERR] = 0;
+        __syncwarp();
         int nv = 0;
         for (int k0 = 0; k0 < kMaxItems; k0 += 32) {
             const int it = blockIdx.x + (k0 + lane) * gridDim.x;
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                     err = GDN_DEV_BAD_NODE_OFF;
                 else if (ns > 0 && (slot < 0 || slot >= a.P))
                     err = GDN_DEV_BAD_SLOT;
-                if (err) gdn::record_status(a.status, err);
+                if (err) words[W_ERR] = err;  // recorded after the wait
             }
             const bool valid = k0 + lane < kMaxItems && it < total && !err && ns > 0;
             const unsigned m = __ballot_sync(0xffffffffu, valid);
@@ -623,6 +628,13 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     const uint32_t tmem = *tmem_slot;
     const int nv = words[W_NV];
     const int nchunks = 4 * nv;
+    if (warp == 0 && lane < kPrefetch + 1 && lane < nv) {
+        const int4 e = list[lane];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) gdn::tma_prefetch_2d(&tmap, 32 * c, (e.w * a.Hv + e.x % a.Hv) * D);
+    }
+    gdn::grid_dep_wait();  // xc, the state pool, status
+    if (tid == 0 && words[W_ERR]) gdn::record_status(a.status, words[W_ERR]);
 
     if (warp == 0) {
         // ---- producer: S0 chunks in order into the ring ----------------------
@@ -635,7 +647,6 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) gdn::tma_prefetch_2d(&tmap, 32 * c, (e.w * a.Hv + e.x % a.Hv) * D);
             };
-            for (int v = 1; v <= kPrefetch; ++v) prefetch_item(v);
             int g = 0;
             for (; g < nchunks; ++g) {
                 const int r = g % NR;
