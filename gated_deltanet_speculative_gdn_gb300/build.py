@@ -27,7 +27,7 @@ BUILD = os.path.join(ROOT, "_build", "gdn_gb300")
 LIB = os.path.join(PKG, "libgdn_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["gdn_api.cpp", "gdn_conv.cu", "gdn_verify.cu", "gdn_chain.cu", "gdn_commit.cu", "gdn_norm.cu", "gdn_decode.cu"]
+SOURCES = ["gdn_api.cpp", "gdn_conv.cu", "gdn_verify.cu", "gdn_chain.cu", "gdn_chain_tc.cu", "gdn_commit.cu", "gdn_norm.cu", "gdn_decode.cu"]
 
 
 def _nvcc() -> str:

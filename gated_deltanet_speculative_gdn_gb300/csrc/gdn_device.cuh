@@ -153,13 +153,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
-// Hint: bring [src, src + bytes) into L2 (16-byte aligned, size a multiple of
-// 16; no shared memory, no completion).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
-
 // ---- tcgen05 (5th-generation tensor cores, accumulators in tensor memory) ----
 
 // Orders this thread's generic-proxy shared-memory writes before later

@@ -57,6 +57,13 @@ inline int check_alias(const Span *outs, int n_out, const Span *ins, int n_in) {
     return GDN_OK;
 }
 
+// Launches the tensor-core chain verify (d = 128) for arguments the entry
+// point has validated; GDN_OK or a host-side error.
+int launch_chain_tc(const gdn_dims *dims, const float *xc, const float *ba, int64_t ba_stride, const float *dt_bias,
+                    const float *A, const float *ssm, float q_scale, const int32_t *parents, const int32_t *node_off,
+                    const int32_t *slot_map, float *o, float *replay, int64_t replay_stride, int32_t *status,
+                    void *stream);
+
 // Bytes of a [rows][stride] float tensor of which the last row holds `width`.
 inline size_t strided_bytes(int64_t rows, int64_t stride, int64_t width) {
     return rows <= 0 ? 0 : static_cast<size_t>(((rows - 1) * stride + width) * 4);

@@ -1202,6 +1202,14 @@ int launch_d(const CUtensorMap &map, const VerifyArgs &a, cudaStream_t st) {
 
 }  // namespace
 
+namespace gdn {
+int encode_xc_tiles(CUtensorMap *map, const float *xc, int64_t N, int64_t C, uint32_t rows, uint32_t cols,
+                    bool swizzle) {
+    return encode_xc_map(map, xc, N, C, rows, cols, swizzle);
+}
+int sm_count_current() { return sm_count(); }
+}  // namespace gdn
+
 extern "C" int gdn_tree_verify(const gdn_dims *dims, const float *xc, const float *ba, int64_t ba_stride,
                                const float *dt_bias, const float *A, const float *ssm, float q_scale,
                                const int32_t *parents, const int32_t *node_off, const int32_t *slot_map,
