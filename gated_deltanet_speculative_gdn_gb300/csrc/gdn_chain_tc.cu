@@ -145,6 +145,13 @@ __device__ __forceinline__ int fp16_exp(float m) {
     if (be == 0) return 0;                                   // zero (or subnormal): no scaling
     return min(14 - (be - 127), 126);
 }
+// Exponent e for the lo parts of values whose largest magnitude is m: every
+// lo part is below 2^(E - 10) when m = 1.f 2^E, so lo 2^e stays below 2^15.
+__device__ __forceinline__ int lo_fp16_exp(float m) {
+    const int be = int((__float_as_uint(m) >> 23) & 0xffu);
+    if (be == 0) return 0;
+    return min(152 - be, 126);
+}
 // 2^e as a float, for -126 <= e <= 127
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
 
@@ -445,14 +452,22 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                 {
                     // quarter-warp = one K-chunk, its eight lanes eight tiles: distinct
                     // rows in one chunk, so the loads avoid bank conflicts
-                    const int kc = (lane >> 3) & 3, tile = (lane & 7) + 8 * (warp - kPrep0);
-                    const int j0 = 4 * (tile & 3), c0 = 4 * (tile >> 2);
+                    // only the 20 tiles the solve reads: row block jb, column block cb
+                    // >= jb of the k columns (k . k), then of the q columns (k . q);
+                    // five per warp, lanes 5-7 of each quarter idle
+                    const int kc = (lane >> 3) & 3, slot = lane & 7;
+                    const int tix = 5 * (warp - kPrep0) + min(slot, 4);
+                    const int grp = tix >= 10, tk = tix - 10 * grp;
+                    const int jb = tk < 4 ? 0 : tk < 7 ? 1 : tk < 9 ? 2 : 3;
+                    const int cbl = jb + (tk - (jb == 0 ? 0 : jb == 1 ? 4 : jb == 2 ? 7 : 9));
+                    const int j0 = 4 * jb, c0 = 4 * cbl + kChunk * grp;
+                    const bool active = slot < 5;
                     const unsigned char *src = tiles + T_BT + kc * kBChunk;
                     float acc[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) acc[q] = 0.f;
 #pragma unroll 2
-                    for (int u = 0; u < 8; ++u) {
+                    for (int u = 0; u < (active ? 8 : 0); ++u) {
                         float4 xc[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) xc[q] = *reinterpret_cast<const float4 *>(src + swz(c0 + q, u));
@@ -476,8 +491,9 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                         acc[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
                     }
                     // this lane: row j0 + kc, columns c0 .. c0 + 3
-                    *reinterpret_cast<float4 *>(fw + S_GR + (j0 + kc) * 32 + c0) =
-                        make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    if (active)
+                        *reinterpret_cast<float4 *>(fw + S_GR + (j0 + kc) * 32 + c0) =
+                            make_float4(acc[0], acc[1], acc[2], acc[3]);
                     if (pt < kChunk) {
                         float qq = 0.f;
 #pragma unroll
@@ -621,11 +637,11 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                         sv[4 * q + 3] = x.w;
                     }
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(lo_part(sv[q])));
+                    for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(sv[q]));
                     tmem_st32(tmem + lanes + TM_S + 32 * b, sv);
                 }
                 tmem_wait_st();
-                const int ex = fp16_exp(mx);
+                const int ex = lo_fp16_exp(mx);
                 const float sc = pow2f(ex);
                 row_unscale = pow2f(-ex);
 #pragma unroll 1
@@ -722,12 +738,16 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                     tmem_st32(tmem + lanes + TM_U, uw);
                     const float gl = cb[C_GAM + L - 1];
 #pragma unroll 1
-                    for (int b = 0; b < 4; ++b) {
-                        float sv[32];
-                        gdn::tmem_ld32(tmem + lanes + TM_S + 32 * b, sv);
+                    for (int b = 0; b < 4; b += 2) {
+                        float sa[32], sb[32];
+                        gdn::tmem_ld32x2(tmem + lanes + TM_S + 32 * b, tmem + lanes + TM_S + 32 * b + 32, sa, sb);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) sv[q] *= gl;
-                        tmem_st32(tmem + lanes + TM_S + 32 * b, sv);
+                        for (int q = 0; q < 32; ++q) {
+                            sa[q] *= gl;
+                            sb[q] *= gl;
+                        }
+                        tmem_st32(tmem + lanes + TM_S + 32 * b, sa);
+                        tmem_st32(tmem + lanes + TM_S + 32 * b + 32, sb);
                     }
                     tmem_wait_st();
                 }
@@ -744,13 +764,13 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                     // chunk's 16-bit product
                     float mx = 0.f;
 #pragma unroll 1
-                    for (int b = 0; b < 4; ++b) {
-                        float sv[32];
-                        gdn::tmem_ld32(tmem + lanes + TM_S + 32 * b, sv);
+                    for (int b = 0; b < 4; b += 2) {
+                        float sa[32], sb[32];
+                        gdn::tmem_ld32x2(tmem + lanes + TM_S + 32 * b, tmem + lanes + TM_S + 32 * b + 32, sa, sb);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(lo_part(sv[q])));
+                        for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fmaxf(fabsf(sa[q]), fabsf(sb[q])));
                     }
-                    const int ex = fp16_exp(mx);
+                    const int ex = lo_fp16_exp(mx);
                     const float sc = pow2f(ex);
                     row_unscale = pow2f(-ex);
 #pragma unroll 1
