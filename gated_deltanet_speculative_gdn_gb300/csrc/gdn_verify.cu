@@ -505,7 +505,8 @@ constexpr int B_BREADY = B_QFULL + 2;      // per team: B's lo rows written (128
 constexpr int B_GFULL = B_BREADY + 2;      // per team: Gram terms complete (1)
 constexpr int B_ACCFULL = B_GFULL + 2;     // per team: accumulators complete (1 from each product issuer)
 constexpr int B_ACCEMPTY = B_ACCFULL + 2;  // per team: accumulators read (128)
-constexpr int B_DRAIN = B_ACCEMPTY + 2;    // the issuers' last tensor-core work done (1 from each)
+constexpr int B_VFULL = B_ACCEMPTY + 2;    // per team: the item's v rows landed in its u tile (1 + bytes)
+constexpr int B_DRAIN = B_VFULL + 2;       // the issuers' last tensor-core work done (1 from each)
 constexpr int B_NEVER = B_DRAIN + 1;       // nothing arrives: the timeout test's wait
 constexpr int N_BARS = B_NEVER + 1;
 constexpr int W_BARS = 2 * T_WORDS;
@@ -557,7 +558,8 @@ __device__ __forceinline__ float4 lo4(float4 x) {
 
 __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     tree_verify_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap xmap,
-                          const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap rmap,
+                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                          const __grid_constant__ CUtensorMap rmap,
                           const VerifyArgs a) {
     using namespace wsv;
     extern __shared__ unsigned char smem_raw[];
@@ -790,7 +792,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         // the sequence's last node belong to the next sequence, or are
         // zero-filled past the tensor: they only feed outputs that are never
         // written)
-        int qk_issued = 0;
+        int qk_issued = 0, v_issued = 0;
         auto issue_qk = [&](int v) {
             if (ttid != 0 || v >= nv) return;
             const int4 e = list[v];
@@ -839,6 +841,15 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             // previous epilogue has finished reading the small area
             if (ttid == 0) gdn::bulk_wait_read0();
             team_sync(team);
+            // the item's 16 v rows by TMA into the u tile (free now: its last
+            // store has read it); the epilogue reads them from there and each
+            // thread writes its u over exactly the entries it read
+            if (ttid == 0) {
+                uint64_t *vb = bars + B_VFULL + team;
+                gdn::mbar_arrive_expect_tx(vb, kSeg * D * 4);
+                gdn::tma_load_2d(stg_u, &vmap, voff, n0, vb);
+                ++v_issued;
+            }
 
             // ---- A: parents and gates (warp 0 of the team: lane = node) -----------
             if (ttid < kSeg) {
@@ -957,16 +968,13 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                                                     4 * lane) = kh;
                 }
             }
-            // v of this thread's row, loaded while the accumulators finish
-            float vreg[kSeg];
-#pragma unroll
-            for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? gdn::ldg_pinned(a.xc + (n0 + t) * int64_t(a.C) + voff + row) : 0.f;
             team_sync(team);  // B is no longer read
 
             // ---- E: per row, r = beta (v - Gamma S0 k^), u = T r, o = Gamma S0 q^ + W r
             // warp-uniform: tcgen05.ld is warp-collective
-            const bool ready =
-                __all_sync(0xffffffffu, wait_or_abort(bars + B_ACCFULL + team, uint32_t(ut & 1), abort_flag));
+            const bool ready = __all_sync(0xffffffffu,
+                                          wait_or_abort(bars + B_ACCFULL + team, uint32_t(ut & 1), abort_flag) &&
+                                              wait_or_abort(bars + B_VFULL + team, uint32_t(ut & 1), abort_flag));
             if (ready) {
                 // the products are done and the team has finished reading B: its
                 // next q/k rows may land there while this epilogue runs
@@ -998,6 +1006,9 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 // Nodes travel as packed pairs (u_2p, u_2p+1), so a column costs
                 // at most 8 paired FMAs and the chain from u_j to u_j+1 is one.
                 // Then o = Gamma S0 q^ + CQ u the same way.
+                float vreg[kSeg];
+#pragma unroll
+                for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? stg_u[t * D + row] : 0.f;
                 uint64_t up[kSeg / 2], op[kSeg / 2];
 #pragma unroll
                 for (int p2 = 0; p2 < kSeg / 2; ++p2) {
@@ -1072,9 +1083,11 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             // once) so that all four warps meet at each team barrier
         }
         if (ttid == 0) gdn::bulk_wait0();  // the last output stores are complete
-        // after a timeout, a q/k copy may still be in flight: wait for it (bounded)
+        // after a timeout, a q/k or v copy may still be in flight: wait for it (bounded)
         if (*abort_flag && qk_issued > 0)
             gdn::mbar_wait_bounded(bars + B_QFULL + team, uint32_t((qk_issued - 1) & 1));
+        if (*abort_flag && v_issued > 0)
+            gdn::mbar_wait_bounded(bars + B_VFULL + team, uint32_t((v_issued - 1) & 1));
     }
 
     // ---- tear-down -------------------------------------------------------------
@@ -1172,8 +1185,9 @@ std::atomic<uint64_t> g_stall_ns{0};
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a_in, cudaStream_t st) {
     VerifyArgs a = a_in;
     a.stall_ns = g_stall_ns.exchange(0);
-    CUtensorMap xmap, omap, rmap;
+    CUtensorMap xmap, vmap, omap, rmap;
     if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C, 16, 32, true)) return rc;
+    if (int rc = encode_xc_map(&vmap, a.xc, a.N, a.C, 16, wsv::D, false)) return rc;
     if (int rc = encode_out_map(&omap, a.o, a.N, a.Hv, wsv::D, wsv::D)) return rc;
     if (int rc = encode_out_map(&rmap, a.replay, a.N, a.Hv, a.rstride, wsv::D)) return rc;
     auto k = tree_verify_ws_kernel;
@@ -1184,7 +1198,7 @@ int launch_tc(const CUtensorMap &map, const VerifyArgs &a_in, cudaStream_t st) {
     if (sms <= 0) return GDN_ERR_LAUNCH;
     // one CTA per SM, each with at most kMaxItems items (more CTAs queue behind)
     int64_t grid = std::max<int64_t>(std::min<int64_t>(items, sms), (items + wsv::kMaxItems - 1) / wsv::kMaxItems);
-    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, omap, rmap, a) == cudaSuccess
+    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, vmap, omap, rmap, a) == cudaSuccess
                ? GDN_OK
                : GDN_ERR_LAUNCH;
 }
