@@ -77,6 +77,20 @@ def test_more_items_than_resident_ctas():
     run_chain(b, lp)
 
 
+def test_more_items_than_one_pass_of_the_grid():
+    """5,200 items of one to three nodes: more than the persistent grid takes
+    in one pass at two CTAs per SM, so the grid grows to keep each CTA's list
+    within its bound."""
+    S, P = 2600, 8
+    sizes = [1 + s % 3 for s in range(S)]
+    b, lp = chain_batch(3350, 1, 2, sizes, P=P, max_nodes=16)
+    b.slot_map = (np.arange(S) % P).astype(np.int32)
+    acc = np.full(S, -1, np.int32)
+    acc[:P] = [sizes[s] - 1 for s in range(P)]
+    b.accepted = acc
+    run_chain(b, lp)
+
+
 def test_chain_kernel_matches_tree_kernel_closely():
     """Both kernels on the same chains: each is within the bar of the oracle,
     and the two agree with each other to the same bar."""
@@ -187,3 +201,38 @@ def test_status_bad_node_offsets_slot_and_length():
     assert chain_status(b, lp)[0] == G.GDN_DEV_BAD_SLOT
     b, lp = chain_batch(43, 1, 2, [40, 6], max_nodes=32)  # 40 > max_seq_nodes
     assert chain_status(b, lp)[0] == G.GDN_DEV_BAD_NODE_OFF
+
+
+def test_contraction_with_full_low_mantissas():
+    """beta = 0 and decay = 1 leave the state at S0 through every chunk, so
+    o_t = S0 q^_t for every node, across chunk boundaries (the state passes
+    through the scale and the rank-16 update with u = 0).  Every S0 and q entry
+    has its low 13 mantissa bits set: the kernel reads the state from tensor
+    memory as its tf32 part and adds the rest from the fp16 lo product, so an
+    operand part that counted those bits twice (or dropped them) would be off
+    by ~2^-11.  The lo product rounds both of its operands to fp16 (11
+    significant bits), so each term is exact to ~2^-20 of |S| |q| (the tree
+    kernel, with exact lo parts of q, to ~2^-21), and the metric's floor at
+    0.1 x RMS magnifies small outputs up to 10x: the bound is 2^-16, against
+    fp64, still far below the ~2^-11 of a wrong split."""
+    from gpu_harness import relerr
+    b, lp = chain_batch(3800, 2, 4, [40, 1, 17])
+    b.ba = np.full_like(b.ba, -100.0)           # sigmoid -> 0, softplus -> 0, decay -> 1
+    xc = run_oracle(b, lp.ssm, lp.conv_hist, commit=False).xc.astype(np.float32)
+    qs = slice(0, b.Hk * D)
+    xc[:, qs] = (xc[:, qs].view(np.uint32) | np.uint32(0x1FFF)).view(np.float32)
+    ssm = np.ascontiguousarray((lp.ssm.view(np.uint32) | np.uint32(0x1FFF)).view(np.float32))
+    pools = GpuPools(ssm, lp.conv_hist)
+    g = run_gpu(b, pools, xc_override=xc, commit=False, chain=True)
+    assert g.status == 0
+    G_ = b.Hv // b.Hk
+    want = np.empty((b.N, b.Hv, D))
+    for s in range(b.S):
+        for t in range(int(b.node_off[s]), int(b.node_off[s + 1])):
+            for h in range(b.Hv):
+                q = xc[t, (h // G_) * D:(h // G_ + 1) * D].astype(np.float64)
+                qhat = q / np.sqrt(np.dot(q, q) + 1e-6)
+                want[t, h] = ssm[b.slot_map[s], h].astype(np.float64) @ qhat
+    err = relerr(g.o, want)
+    print(f"o = S0 q^ over chunks: {err:.2e}")
+    assert err <= 2.0 ** -16, err
