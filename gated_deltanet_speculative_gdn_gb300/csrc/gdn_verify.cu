@@ -734,12 +734,29 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             gdn::mbar_wait_bounded(bars + B_DRAIN, 0);
         }
     } else if (warp >= kSplit0) {
-        // ---- splitters, chunks in order: once a chunk's A_hi products have read
-        //      it, each 16-byte unit is replaced by its lo part (an elementwise
-        //      pass in the chunk's own swizzled layout). -------------------------
+        // ---- splitters, items in order: as soon as an item's q/k rows land in
+        //      its team's B, the lo rows of B (so that the Gram and product
+        //      issuers can start while the team still runs its previous
+        //      epilogue); then, once each S0 chunk's A_hi products have read it,
+        //      the chunk's lo part in place (elementwise, in the chunk's own
+        //      swizzled layout). -------------------------------------------------
         const int st = tid - kSplit0 * 32;
         for (int g = 0; g < nchunks; ++g) {
             const int r = g % NR;
+            if ((g & 3) == 0) {
+                const int v = g >> 2, t = v & 1;
+                if (!wait_or_abort(bars + B_QFULL + t, uint32_t((v >> 1) & 1), abort_flag)) break;
+                unsigned char *bt = sb + BT + t * kBTeam;
+#pragma unroll
+                for (int j = 0; j < (4 * 32 * 8) / kSplitThreads; ++j) {
+                    const int idx = st + kSplitThreads * j;  // 16-byte unit: K-chunk idx / 256, rows 0-31
+                    unsigned char *p = bt + (idx >> 8) * kBChunk + (idx & 255) * 16;
+                    const float4 x = *reinterpret_cast<const float4 *>(p);
+                    *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
+                }
+                gdn::fence_proxy_async_smem();
+                mbar_arrive(bars + B_BREADY + t);
+            }
             if (!wait_or_abort(bars + B_HDONE + r, uint32_t((g / NR) & 1), abort_flag)) break;
             float4 *c = reinterpret_cast<float4 *>(sb + RAW + r * kChunk);
             constexpr int kPer = int(kChunk / 16) / kSplitThreads;  // 16-byte units per thread
@@ -807,23 +824,6 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             ++qk_issued;
         };
         issue_qk(team);
-        // the team writes the lo rows of its next item's B as soon as the rows
-        // land (the Gram and product issuers wait for them)
-        auto split_b = [&](int v) -> bool {
-            if (v >= nv) return false;
-            if (!wait_or_abort(bars + B_QFULL + team, uint32_t((v >> 1) & 1), abort_flag)) return false;
-#pragma unroll
-            for (int j = 0; j < (4 * 32 * 8) / 128; ++j) {
-                const int idx = ttid + 128 * j;  // 16-byte unit: K-chunk idx / 256, rows 0-31
-                unsigned char *p = bt_t + (idx >> 8) * kBChunk + (idx & 255) * 16;
-                const float4 x = *reinterpret_cast<const float4 *>(p);
-                *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
-            }
-            gdn::fence_proxy_async_smem();
-            mbar_arrive(bars + B_BREADY + team);
-            return true;
-        };
-        bool staged_nx = split_b(team);
         // test hook: team 0 of CTA 0 waits on a barrier that nothing completes,
         // so the wait runs out, and every role drains and leaves
         if (a.stall_ns && blockIdx.x == 0 && team == 0 &&
@@ -897,10 +897,11 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             //      16 tw + 15 (k, q, k_lo, q_lo of the nodes) in lanes 0..15, columns
             //      [k | q | k_lo | q_lo]: a row against column j plus column 32 + j is
             //      its dot product with all of k_j. ----------------------------------
-            const bool staged = staged_nx;
-            // warp-uniform: tcgen05.ld is warp-collective
+            // warp-uniform: tcgen05.ld is warp-collective.  The Gram terms
+            // complete after the splitters wrote B's lo rows, so B is in place
             const bool gready =
-                __all_sync(0xffffffffu, staged && wait_or_abort(bars + B_GFULL + team, uint32_t(ut & 1), abort_flag));
+                __all_sync(0xffffffffu, wait_or_abort(bars + B_GFULL + team, uint32_t(ut & 1), abort_flag));
+            const bool staged = gready;
             if (gready) {
                 gdn::tc_fence_after_sync();
                 const uint32_t grow = tmem + TEAM_COLS * team + GCOL + (uint32_t(tw * 32) << 16);
@@ -1076,9 +1077,6 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                     gdn::bulk_commit_group();
                 }
             }
-            // the lo rows of the next item's B (its q/k rows were requested when
-            // this item's accumulators completed and have landed meanwhile)
-            staged_nx = ready && split_b(v + 2);
             // after a timeout the team keeps looping (every wait now returns at
             // once) so that all four warps meet at each team barrier
         }
