@@ -323,6 +323,7 @@ def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int
            "clocks": sampler.summary() if sampler else None}
     if e2e:
         out["e2e"] = time_e2e(wl, steps, warmup)
+        out["e2e_overlapped"] = time_e2e_overlapped(wl, steps, warmup)
     return out
 
 
@@ -362,6 +363,63 @@ def time_e2e(wl: DeviceWorkload, steps: int, warmup: int, host_rounds: int = 8):
         times.append(a.elapsed_time(b))
     ms = statistics.mean(times)
     return {"ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def time_e2e_overlapped(wl: DeviceWorkload, steps: int, warmup: int, host_rounds: int = 8):
+    """The same steps through the C ABI from pinned host buffers with the copies
+    on their own streams: step i's inputs go up (one copy stream) while step
+    i - 1 computes and step i - 2's output comes back (a second copy stream),
+    with double-buffered device inputs and outputs and events between the
+    streams.  Every step's copies are inside the timed region; the figure is
+    whole-run throughput (no L2 flush between steps: the three streams run
+    concurrently)."""
+    import torch
+    nr = min(host_rounds, len(wl.rounds))
+    host = [{k: v.cpu().pin_memory() for k, v in wl.rounds[r].items()} for r in range(nr)]
+    dev_in = [{k: torch.empty_like(v) for k, v in wl.rounds[0].items()} for _ in range(2)]
+    o_dev = [wl.o, torch.empty_like(wl.o)]
+    o_host = [torch.empty(wl.o.shape, dtype=wl.o.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = wl.o.numel() * wl.o.element_size()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev() for _ in range(2)]
+    in_free = [ev() for _ in range(2)]
+    done = [ev() for _ in range(2)]
+    out_free = [ev() for _ in range(2)]
+    for e in in_free + out_free:
+        e.record(comp)
+
+    def run(i0, n):
+        for i in range(i0, i0 + n):
+            b, r = i % 2, i % nr
+            with torch.cuda.stream(up):
+                up.wait_event(in_free[b])
+                for k, v in host[r].items():
+                    dev_in[b][k].copy_(v, non_blocking=True)
+                in_ready[b].record(up)
+            comp.wait_event(in_ready[b])
+            comp.wait_event(out_free[b])
+            wl.o = o_dev[b]
+            wl.step(r, None, dev_in[b])
+            in_free[b].record(comp)
+            done[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done[b])
+                o_host[b].copy_(o_dev[b], non_blocking=True)
+                out_free[b].record(down)
+
+    run(0, warmup)
+    torch.cuda.synchronize()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    run(warmup, steps)
+    comp.wait_stream(down)
+    z.record(comp)
+    torch.cuda.synchronize()
+    wl.o = o_dev[0]
+    return {"ms_per_step": a.elapsed_time(z) / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 def time_config(index: int, steps: int, warmup: int, device):
@@ -662,10 +720,11 @@ def main():
     N = head["wl"].N
     step_ms = statistics.mean(head["step_ms"])
     e2e_ms = head["e2e"]["ms_per_step"]
+    e2e_ov_ms = head["e2e_overlapped"]["ms_per_step"]
     if dist is not None:
-        t = torch.tensor([step_ms, e2e_ms], device=device)
+        t = torch.tensor([step_ms, e2e_ms, e2e_ov_ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+        step_ms, e2e_ms, e2e_ov_ms = float(t[0]), float(t[1]), float(t[2])
         dist.barrier()
     if rank != 0:
         if dist is not None:
@@ -746,6 +805,13 @@ def main():
                 "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": head["e2e"]["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": head["e2e"]["d2h_bytes_per_step"]},
+        "e2e_overlapped": {"value": round(nodes_total / (e2e_ov_ms * 1e-3), 1),
+                           "unit": "nodes/s", "ms_per_step": round(e2e_ov_ms, 5),
+                           "h2d_bytes_per_step": head["e2e_overlapped"]["h2d_bytes_per_step"],
+                           "d2h_bytes_per_step": head["e2e_overlapped"]["d2h_bytes_per_step"],
+                           "note": "the same C-ABI steps with the input copy (one stream), the step (another) "
+                                   "and the output copy (a third) of consecutive steps overlapped through "
+                                   "double-buffered device buffers and events; e2e above is the serial figure"},
         "gpu_launches": 4 * args.steps * (1 + len(others)),
         "gpu_launches_note": "timed head steps x 4 launches (conv, verify, commit preflight, commit apply); "
                              "the second whole-step pass and the sweep variants launch the same per step",
