@@ -75,7 +75,7 @@ constexpr int C_RQ = C_RK + 16;          //   [16] 1/|q_t|
 constexpr int C_FS = C_RQ + 16;          //   [32] 2^-f of the fp16 copy of raw row c of [k | q]
 constexpr int C_WORDS = C_FS + 32;
 constexpr int S_BAR = (S_CB + 2 * C_WORDS + 1) & ~1;
-enum { B_LAND, B_BLO, B_PREP, B_KT, B_BFREE, B_DHI, B_DLO, B_DFREE, B_UPRDY, B_UDONE, B_SRDY, B_DRAIN, N_BARS };
+enum { B_LAND, B_BLO, B_PREP, B_KT, B_BFREE, B_DHI, B_DLO, B_DFREE, B_UPRDY, B_UDONE, B_SRDY, B_DRAIN, B_NEVER, N_BARS };
 constexpr int S_TMEM = S_BAR + 2 * N_BARS;
 constexpr int S_ABORT = S_TMEM + 1;
 constexpr int S_NV = S_ABORT + 1;
@@ -194,6 +194,7 @@ struct ChainTcArgs {
     int64_t rstride;
     int32_t *status;
     int S, N, P, Hk, Hv, C, max_nodes;
+    uint64_t stall_ns;  // test hook: a wait that nothing ends, for this long (0: none)
 };
 
 __global__ void __launch_bounds__(ctc::kThreads, 2)
@@ -282,6 +283,13 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
         if (lane == 0) {
             int g = 0, last_land = -1;
             bool ok = true;
+            // test hook: the producer of CTA 0 waits on a barrier that nothing
+            // completes, so the wait runs out before any copy is issued, and
+            // every other role's wait runs out in turn
+            if (a.stall_ns && blockIdx.x == 0 && !gdn::mbar_wait_bounded(bars + B_NEVER, 0, a.stall_ns)) {
+                *abort_flag = 1;
+                ok = false;
+            }
             for (int v = 0; v < nv && ok; ++v) {
                 const int4 e = list[v];
                 const int h = e.x % a.Hv, kh = h / G;
@@ -813,7 +821,7 @@ int launch_chain_tc(const gdn_dims *dims, const float *xc, const float *ba, int6
     if (int rc = gdn::encode_xc_tiles(&xmap, xc, N, C, kChunk, 32, true)) return rc;
     const ChainTcArgs a{xc, ba, ba_stride, dt_bias, A, ssm, q_scale, parents, node_off, slot_map, o, replay,
                         replay_stride, status, int(S), int(N), dims->n_slots, dims->h_k, int(Hv), int(C),
-                        dims->max_seq_nodes};
+                        dims->max_seq_nodes, gdn::take_test_stall_ns()};
     auto k = chain_verify_tc_kernel;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;

@@ -64,6 +64,10 @@ int launch_chain_tc(const gdn_dims *dims, const float *xc, const float *ba, int6
                     const int32_t *slot_map, float *o, float *replay, int64_t replay_stride, int32_t *status,
                     void *stream);
 
+// The pending test stall of gdn_test_stall_next_verify (ns, 0: none); taking
+// it clears it, so exactly one tensor-core verify launch receives it.
+uint64_t take_test_stall_ns();
+
 // Bytes of a [rows][stride] float tensor of which the last row holds `width`.
 inline size_t strided_bytes(int64_t rows, int64_t stride, int64_t width) {
     return rows <= 0 ? 0 : static_cast<size_t>(((rows - 1) * stride + width) * 4);

@@ -1182,7 +1182,7 @@ std::atomic<uint64_t> g_stall_ns{0};
 
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a_in, cudaStream_t st) {
     VerifyArgs a = a_in;
-    a.stall_ns = g_stall_ns.exchange(0);
+    a.stall_ns = gdn::take_test_stall_ns();
     CUtensorMap xmap, vmap, omap, rmap;
     if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C, 16, 32, true)) return rc;
     if (int rc = encode_xc_map(&vmap, a.xc, a.N, a.C, 16, wsv::D, false)) return rc;
@@ -1220,6 +1220,7 @@ int encode_xc_tiles(CUtensorMap *map, const float *xc, int64_t N, int64_t C, uin
     return encode_xc_map(map, xc, N, C, rows, cols, swizzle);
 }
 int sm_count_current() { return sm_count(); }
+uint64_t take_test_stall_ns() { return g_stall_ns.exchange(0); }
 }  // namespace gdn
 
 extern "C" int gdn_tree_verify(const gdn_dims *dims, const float *xc, const float *ba, int64_t ba_stride,

@@ -277,14 +277,17 @@ int gdn_decode_step(const gdn_dims *dims, const float *x, int64_t x_stride, cons
                     const float *A, float *ssm, float q_scale, const int32_t *slot_map, float *xc,
                     float *o, int32_t *status, void *stream);
 
-/* Test hook for the device timeout path.  The next gdn_tree_verify call that
- * runs the tensor-core kernel (d = 128, max_seq_nodes <= 16) makes one team of
- * its first CTA wait on a barrier that nothing ever completes, for wait_ns
- * (capped at the library's 2 s wait limit); the wait runs out, every role of
- * that CTA drains its copies and tensor-core work and leaves, and the call
- * reports GDN_DEV_TIMEOUT in *status (its outputs are then unspecified).  The
- * hook is consumed by that one call.  The paper has no counterpart; it exists
- * so that the bounded-wait path can be tested without a GPU fault. */
+/* Test hook for the device timeout path.  The next call that runs a
+ * tensor-core verify kernel (gdn_tree_verify with d = 128 and
+ * max_seq_nodes <= 16, or gdn_chain_verify) makes one role of its first CTA
+ * wait on a barrier that nothing ever completes, for wait_ns (capped at the
+ * library's 2 s wait limit); the wait runs out, every role of that CTA drains
+ * its copies and tensor-core work and leaves (the chain kernel's other roles
+ * each wait out their own limit first, so that call takes about 2 s), and the
+ * call reports GDN_DEV_TIMEOUT in *status (its outputs are then unspecified).
+ * The hook is consumed by that one call; calls that run another kernel leave
+ * it pending.  The paper has no counterpart; it exists so that the bounded-wait
+ * path can be tested without a GPU fault. */
 void gdn_test_stall_next_verify(uint64_t wait_ns);
 
 /* Name of a host or device status code ("GDN_OK", "GDN_DEV_DUP_SLOT", ...);

@@ -194,3 +194,38 @@ def compare(g: GpuOut, r: OracleOut, tol: float = TOL, check_xc: bool = True):
     for k, v in errs.items():
         assert v <= tol, (k, v)
     return errs
+
+
+def custom_batch(seed, Hk, Hv, d, sizes, P=None, kind="tree", forest=False, max_nodes=None,
+                 accepted=None):
+    """A batch of ragged sequences with the given node counts: random trees
+    (or chains, kind="chain"; forest=True makes every fifth node a root),
+    seeded inputs, the accepted node drawn per sequence unless given."""
+    S = len(sizes)
+    P = P or 2 * S + 1
+    sp = W.Spec(f"edge{seed}", W.Shape(S, P, Hk, Hv, d), "tree", list(sizes), seed)
+    lp = W.layer_params(sp)
+    sm = W.slot_map(sp)
+    off = np.zeros(S + 1, np.int32)
+    off[1:] = np.cumsum(sizes)
+    N = int(off[-1])
+    parents = np.empty(N, np.int32)
+    acc = np.empty(S, np.int32)
+    for s, ns in enumerate(sizes):
+        st = W.Stream(seed, 0, W.TID_TREE, 0, s)
+        if kind == "chain":
+            par = [i - 1 for i in range(ns)]
+        else:
+            par = W.random_tree(st, ns, 8 if ns <= 24 else 64, 3)
+        if forest:
+            par = [-1 if (i % 5 == 0) else p for i, p in enumerate(par)]
+        parents[off[s]:off[s + 1]] = par
+        acc[s] = -1 if ns == 0 else int(W.Stream(seed, 0, W.TID_ACC, 0, s).randint(1, ns + 1)[0]) - 1
+    if accepted is not None:
+        acc[:] = accepted
+    C = 2 * Hk * d + Hv * d
+    x = W.Stream(seed, 0, W.TID_X, 0).normal(N * C).reshape(N, C)
+    ba = W.Stream(seed, 0, W.TID_BA, 0).normal(N * 2 * Hv).reshape(N, 2 * Hv)
+    b = Batch(S, P, Hk, Hv, d, max_nodes or (16 if max(sizes) <= 16 else 64), x, ba, parents, off, sm,
+              acc, lp.conv_w, lp.dt_bias, lp.A)
+    return b, lp

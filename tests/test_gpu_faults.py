@@ -6,8 +6,7 @@ import pytest
 import torch
 
 import gated_deltanet_speculative_gdn_gb300 as G
-from gpu_harness import GpuPools, dev, run_gpu
-from test_gpu_parity import custom_batch
+from gpu_harness import GpuPools, custom_batch, dev, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -112,4 +111,27 @@ def test_verify_wait_that_runs_out_reports_timeout_and_the_context_survives():
     assert g.status == G.GDN_DEV_TIMEOUT, G.gdn_status_str(g.status)
     assert_pools_unchanged(pools, lp)
     g2 = run_gpu(b, pools)
+    compare(g2, run_oracle(b, lp.ssm, lp.conv_hist))
+
+
+def test_chain_verify_wait_that_runs_out_reports_timeout_and_the_context_survives():
+    """The same hook on the chain kernel: a d = 64 tree round first runs
+    another kernel and leaves the hook pending (its result is exact); the
+    chain round that follows takes it, the producer of its first CTA gives up
+    before issuing a copy, the other roles' waits run out in turn, *status
+    reads GDN_DEV_TIMEOUT and the commit writes nothing.  The next chain round
+    on the same context is exact."""
+    from gpu_harness import compare, run_oracle
+    bt, lt = custom_batch(19, 2, 4, 64, [16, 7])
+    G.gdn_test_stall_next_verify(20_000_000)
+    pt = GpuPools(lt.ssm, lt.conv_hist)
+    gt = run_gpu(bt, pt)
+    assert gt.status == 0, G.gdn_status_str(gt.status)
+    compare(gt, run_oracle(bt, lt.ssm, lt.conv_hist))
+    b, lp = custom_batch(20, 2, 4, 128, [40, 23, 16], kind="chain", max_nodes=64)
+    pools = GpuPools(lp.ssm, lp.conv_hist)
+    g = run_gpu(b, pools, chain=True)
+    assert g.status == G.GDN_DEV_TIMEOUT, G.gdn_status_str(g.status)
+    assert_pools_unchanged(pools, lp)
+    g2 = run_gpu(b, pools, chain=True)
     compare(g2, run_oracle(b, lp.ssm, lp.conv_hist))

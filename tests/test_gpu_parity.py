@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import gdn_workloads as W
-from gpu_harness import (TOL, Batch, GpuPools, batch_from, compare, relerr, run_gpu, run_oracle)
+from gpu_harness import (TOL, Batch, GpuPools, batch_from, compare, custom_batch, relerr, run_gpu,
+                         run_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -86,38 +87,6 @@ def test_sweep_full_size_three_rounds(variant):
 
 
 # ---------------------------------------------------------------- edge cases
-def custom_batch(seed, Hk, Hv, d, sizes, P=None, kind="tree", forest=False, max_nodes=None,
-                 accepted=None):
-    S = len(sizes)
-    P = P or 2 * S + 1
-    sp = W.Spec(f"edge{seed}", W.Shape(S, P, Hk, Hv, d), "tree", list(sizes), seed)
-    lp = W.layer_params(sp)
-    sm = W.slot_map(sp)
-    off = np.zeros(S + 1, np.int32)
-    off[1:] = np.cumsum(sizes)
-    N = int(off[-1])
-    parents = np.empty(N, np.int32)
-    acc = np.empty(S, np.int32)
-    for s, ns in enumerate(sizes):
-        st = W.Stream(seed, 0, W.TID_TREE, 0, s)
-        if kind == "chain":
-            par = [i - 1 for i in range(ns)]
-        else:
-            par = W.random_tree(st, ns, 8 if ns <= 24 else 64, 3)
-        if forest:
-            par = [-1 if (i % 5 == 0) else p for i, p in enumerate(par)]
-        parents[off[s]:off[s + 1]] = par
-        acc[s] = -1 if ns == 0 else int(W.Stream(seed, 0, W.TID_ACC, 0, s).randint(1, ns + 1)[0]) - 1
-    if accepted is not None:
-        acc[:] = accepted
-    C = 2 * Hk * d + Hv * d
-    x = W.Stream(seed, 0, W.TID_X, 0).normal(N * C).reshape(N, C)
-    ba = W.Stream(seed, 0, W.TID_BA, 0).normal(N * 2 * Hv).reshape(N, 2 * Hv)
-    b = Batch(S, P, Hk, Hv, d, max_nodes or (16 if max(sizes) <= 16 else 64), x, ba, parents, off, sm,
-              acc, lp.conv_w, lp.dt_bias, lp.A)
-    return b, lp
-
-
 def run_edge(b, lp, q_scale=1.0, **kw):
     pools = GpuPools(lp.ssm, lp.conv_hist)
     g = run_gpu(b, pools, q_scale=q_scale, **kw)
