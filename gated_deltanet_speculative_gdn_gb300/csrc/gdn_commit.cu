@@ -25,6 +25,7 @@
 //             the slot's conv history.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
+#include "gdn_tma.h"
 
 namespace {
 
@@ -269,6 +270,376 @@ __global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const
     }
 }
 
+// Streaming apply for d = 128: a persistent CTA per SM walks the committing
+// units of its share, a unit being 64 state rows (32 KB, half of one head's
+// state).  The tile and the path's replay rows (k^_j and the unit's half of
+// u_j) arrive by bulk copies into a ring of kStages stages, so each SM keeps
+// well over 100 KB of state in flight while it applies earlier units.  A stage
+// holds kEntries path entries; a longer path passes through in batches, each
+// batch one more phase of the stage's barriers.
+//
+// Producer warp p fills stage p for every kStages-th committing unit.  It finds
+// its units with a warp-wide scan of `accepted` (one lane per unit, a ballot),
+// walks the path (parents two per lane, shuffles), reads the path's decays,
+// forms Gamma and the closed-form coefficients with a warp scan, leaves the
+// unit, the path and the coefficients in the stage's small area, issues the
+// copies, and copies the unit's share of the accepted window into the conv
+// history.  Its first unit's walk needs only the caller's index inputs and
+// runs before the launch wait.  After the last unit, the producer of the next
+// stage in line leaves an end marker there.
+//
+// Sixteen consumer warps take the stages in ring order and learn everything
+// from the stage itself: warp w owns rows 4 w .. 4 w + 3 of the unit (lane l:
+// float4 column group l), loads them times Gamma, adds the path's rank-1 terms
+// root first and stores them with coalesced 128-bit stores.
+namespace cst {
+constexpr int D = 128;
+constexpr int kUnitRows = 64;                   // state rows per unit
+constexpr int kEntryFloats = D + kUnitRows;     // k^_j | the unit's 64 entries of u_j
+constexpr uint32_t kTileBytes = kUnitRows * D * 4;
+constexpr uint32_t kEntryBytes = kEntryFloats * 4;
+constexpr int kConsumerWarps = kUnitRows / 4;
+// per-stage small area (4-byte words)
+constexpr int SM_M = 0;                         // path length; 0: nothing to apply; -1: no more units
+constexpr int SM_GAM = 1;                       // Gamma, the product of the path's decays
+constexpr int SM_SLOT = 2;
+constexpr int SM_HH = 3;                        // 2 h + half
+constexpr int SM_COEF = 4;                      // [64] coefficient of leaf-first entry i
+constexpr int SM_NODE = SM_COEF + gdn::kMaxSeqNodes;  // [64] leaf-first entry i's node
+constexpr int SM_WORDS = SM_NODE + gdn::kMaxSeqNodes;
+
+// The ring: kStages stages (= producer warps) of one tile and kEntries path
+// entries each.  Five stages of 16 entries when no path is longer than 16
+// (trees of up to 16 nodes); four of 32 otherwise, so that long paths (chains)
+// pass in fewer batches.
+template <int kStages_, int kEntries_>
+struct Ring {
+    static constexpr int kStages = kStages_, kEntries = kEntries_;
+    static constexpr uint32_t kStageBytes = kTileBytes + kEntries * kEntryBytes;
+    static constexpr int kThreads = 32 * (kConsumerWarps + kStages);
+    static constexpr size_t SMALL_OFF = size_t(kStages) * kStageBytes;
+    static constexpr size_t BAR_OFF = SMALL_OFF + size_t(kStages) * SM_WORDS * 4;
+    static constexpr size_t BYTES = BAR_OFF + 2 * kStages * 8 + 16;
+    static_assert(BYTES <= 227 * 1024, "shared memory");
+    static_assert(kStageBytes % 16 == 0 && kEntryBytes % 16 == 0 && BAR_OFF % 8 == 0, "16-byte copies");
+    static_assert(kEntries <= 32, "one lane per staged entry");
+};
+using RingShort = Ring<5, 16>;
+using RingLong = Ring<4, 32>;
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (*abort_flag) return false;
+    if (gdn::mbar_wait_bounded(bar, parity)) return true;
+    *abort_flag = 1;
+    return false;
+}
+__device__ __forceinline__ void arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gdn::smem_addr(bar)) : "memory");
+}
+// entries of batch b of a path of m: root first, leaf-first indices
+// m - 1 - kEntries b down to m - kEntries (b + 1), staging slots 0, 1, ...
+template <int kEntries>
+__device__ __forceinline__ int batch_count(int m, int b) { return min(kEntries, m - kEntries * b); }
+
+// A producer's view of its units: the CTA's units u = blockIdx.x + k gridDim.x
+// are scanned 32 at a time; committing units are numbered in order, and
+// producer p takes those numbered p, p + kStages, ...
+struct UnitScan {
+    int64_t next_k = 0;   // first CTA-unit index of the next chunk to scan
+    unsigned mine = 0;    // this producer's units left in the current chunk (lane bits)
+    int64_t chunk_k = 0;  // CTA-unit index of lane 0 of the current chunk
+    int live = 0;         // committing units in the chunks scanned so far
+};
+// Next unit of producer p, or -1; warp-uniform.
+template <int kStages>
+__device__ __forceinline__ int64_t next_unit(UnitScan &sc, const CommitArgs &a, int64_t units, int p, int lane) {
+    while (!sc.mine) {
+        const int64_t k0 = sc.next_k;
+        if (blockIdx.x + k0 * gridDim.x >= units) return -1;
+        const int64_t u = blockIdx.x + (k0 + lane) * gridDim.x;
+        const bool live = u < units && a.accepted[u / (2 * a.Hv)] >= 0;
+        const unsigned lm = __ballot_sync(0xffffffffu, live);
+        const int idx = sc.live + __popc(lm & ((1u << lane) - 1u));  // committing-unit number of this lane
+        sc.mine = __ballot_sync(0xffffffffu, live && idx % kStages == p);
+        sc.live += __popc(lm);
+        sc.chunk_k = k0;
+        sc.next_k = k0 + 32;
+    }
+    const int l = __ffs(sc.mine) - 1;
+    sc.mine &= sc.mine - 1;
+    return blockIdx.x + (sc.chunk_k + l) * gridDim.x;
+}
+
+// The path of unit u (leaf first: entry i's node in lane i % 32 of node_lo /
+// node_hi), from the caller's index inputs only.
+struct Path {
+    int s, h, half, acc, n0, slot, m, node_lo, node_hi;
+    bool bad;
+};
+__device__ __forceinline__ Path walk_path(const CommitArgs &a, int64_t u, int lane) {
+    Path q;
+    q.s = int(u / (2 * a.Hv));
+    q.h = int((u >> 1) % a.Hv);
+    q.half = int(u & 1);
+    q.acc = a.accepted[q.s];
+    q.n0 = a.node_off[q.s];
+    const int n1 = a.node_off[q.s + 1];
+    q.slot = a.slot_map[q.s];
+    // the preflight has checked every index (the status is zero); these tests
+    // only keep the loads below in bounds
+    q.bad = !(q.n0 >= 0 && n1 <= a.N && n1 - q.n0 <= gdn::kMaxSeqNodes && q.acc < n1 - q.n0 && q.slot >= 0 &&
+              q.slot < a.P);
+    q.node_lo = q.node_hi = -1;
+    q.m = 0;
+    if (!q.bad) {
+        const int p_lo = lane <= q.acc ? a.parents[q.n0 + lane] : -1;
+        const int p_hi = lane + 32 <= q.acc ? a.parents[q.n0 + lane + 32] : -1;
+        for (int cur = q.acc; cur >= 0 && q.m < gdn::kMaxSeqNodes; ++q.m) {
+            if (lane == (q.m & 31)) {
+                if (q.m < 32) q.node_lo = cur; else q.node_hi = cur;
+            }
+            const int nx = __shfl_sync(0xffffffffu, cur < 32 ? p_lo : p_hi, cur & 31);
+            q.bad |= nx >= cur;  // parents precede their children
+            cur = nx;
+        }
+    }
+    if (q.bad) q.m = 0;
+    return q;
+}
+}  // namespace cst
+
+template <class R>
+__global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const CommitArgs a) {
+    using namespace cst;
+    constexpr int kStages = R::kStages, kEntries = R::kEntries;
+    constexpr uint32_t kStageBytes = R::kStageBytes;
+    constexpr size_t SMALL_OFF = R::SMALL_OFF, BAR_OFF = R::BAR_OFF;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    int *small = reinterpret_cast<int *>(smem_raw + SMALL_OFF);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + BAR_OFF);
+    uint64_t *empty = full + kStages;
+    volatile int *abort_flag = reinterpret_cast<int *>(full + 2 * kStages);  // [1]: the status was not zero
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned all = 0xffffffffu;
+    const int64_t units = int64_t(a.S) * a.Hv * 2;
+    const int64_t rnode = int64_t(a.Hv) * a.rstride;
+
+    gdn::grid_dep_launch();
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            gdn::mbar_init(full + i, 1);
+            gdn::mbar_init(empty + i, kConsumerWarps);
+        }
+        gdn::fence_mbar_init();
+        *abort_flag = 0;
+    }
+    __syncthreads();
+
+    if (warp >= kConsumerWarps) {
+        // ---- producer warp p: every kStages-th committing unit, into stage p ----
+        const int p = warp - kConsumerWarps;
+        uint64_t *fb = full + p;
+        int *sa = small + p * SM_WORDS;
+        float *sf = reinterpret_cast<float *>(sa);
+        unsigned char *stage = smem_raw + size_t(p) * kStageBytes;
+        float *ent = reinterpret_cast<float *>(stage + kTileBytes);
+        UnitScan sc;
+        int ph = 0;  // phases of stage p issued
+        bool ok = true;
+        int64_t u = next_unit<kStages>(sc, a, units, p, lane);
+        Path q = walk_path(a, u >= 0 ? u : 0, lane);  // before the wait: index inputs only
+        gdn::grid_dep_wait();  // status, the state pool, the replay rows and the windows
+        // one reading of the status for the whole CTA: not zero, nothing is committed
+        if (p == 0 && lane == 0) abort_flag[1] = *reinterpret_cast<volatile int32_t *>(a.status) != 0;
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kStages) : "memory");
+        const bool failed = abort_flag[1] != 0;
+        if (failed) u = -1;
+        while (u >= 0 && ok) {
+            // coefficient of leaf-first entry i = product of the decays of entries 0 .. i-1
+            const float *row0 = a.replay + (int64_t(q.n0) * a.Hv + q.h) * a.rstride;
+            const float d_lo = q.m && q.node_lo >= 0 ? __ldg(row0 + q.node_lo * rnode + 2 * D) : 1.0f;
+            const float d_hi = q.m && q.node_hi >= 0 ? __ldg(row0 + q.node_hi * rnode + 2 * D) : 1.0f;
+            float x_lo = d_lo, x_hi = d_hi;  // inclusive scans
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y_lo = __shfl_up_sync(all, x_lo, o), y_hi = __shfl_up_sync(all, x_hi, o);
+                if (lane >= o) {
+                    x_lo *= y_lo;
+                    x_hi *= y_hi;
+                }
+            }
+            const float tot_lo = __shfl_sync(all, x_lo, 31);
+            float c_lo = __shfl_up_sync(all, x_lo, 1), c_hi = __shfl_up_sync(all, x_hi, 1);
+            if (lane == 0) {
+                c_lo = 1.0f;
+                c_hi = 1.0f;
+            }
+            c_hi *= tot_lo;
+            const float gam = tot_lo * __shfl_sync(all, x_hi, 31);
+            const int m = q.m;
+            const int nb = m ? (m + kEntries - 1) / kEntries : 1;
+            for (int b = 0; b < nb; ++b) {
+                // the stage's previous phase has been read by every consumer warp
+                if (!__all_sync(all, ph == 0 || wait_or_abort(empty + p, uint32_t((ph - 1) & 1), abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                ++ph;
+                if (b == 0) {
+                    if (lane < m) {
+                        sa[SM_COEF + lane] = __float_as_int(c_lo);
+                        sa[SM_NODE + lane] = q.node_lo;
+                    }
+                    if (lane + 32 < m) {
+                        sa[SM_COEF + lane + 32] = __float_as_int(c_hi);
+                        sa[SM_NODE + lane + 32] = q.node_hi;
+                    }
+                    if (lane == 0) {
+                        sa[SM_M] = m;
+                        sf[SM_GAM] = gam;
+                        sa[SM_SLOT] = q.slot;
+                        sa[SM_HH] = 2 * q.h + q.half;
+                    }
+                    __threadfence_block();
+                }
+                __syncwarp();
+                const int cnt = m ? batch_count<kEntries>(m, b) : 0;
+                if (lane == 0)
+                    gdn::mbar_arrive_expect_tx(fb, (b == 0 && m ? kTileBytes : 0) + cnt * kEntryBytes);
+                __syncwarp();
+                if (b == 0 && m && lane == 0)
+                    gdn::bulk_load(stage, a.ssm + ((int64_t(q.slot) * a.Hv + q.h) * D + kUnitRows * q.half) * D,
+                                   kTileBytes, fb);
+                if (lane < cnt) {
+                    const float *rr = row0 + sa[SM_NODE + m - 1 - kEntries * b - lane] * rnode;
+                    float *dst = ent + lane * kEntryFloats;
+                    gdn::bulk_load(dst, rr, D * 4, fb);
+                    gdn::bulk_load(dst + D, rr + D + kUnitRows * q.half, kUnitRows * 4, fb);
+                }
+            }
+            if (ok && m) {
+                // this unit's share of the history copy, conv_hist[slot] <- window of the accepted node
+                const int64_t parts = int64_t(a.Hv) * 2;
+                float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(q.slot) * 3 * a.C);
+                if (!a.wref) {
+                    const int64_t total4 = int64_t(3) * a.C / 4, per = (total4 + parts - 1) / parts;
+                    const int64_t lo = (2 * int64_t(q.h) + q.half) * per, hi = min(total4, lo + per);
+                    const float4 *wsrc =
+                        reinterpret_cast<const float4 *>(a.win + (int64_t(q.n0) + q.acc) * 3 * a.C);
+                    for (int64_t i = lo + lane; i < hi; i += 32) hdst[i] = __ldg(wsrc + i);
+                } else {
+                    // compact form: gathered through the accepted node's references from
+                    // x rows and the slot's old history; a lane reads all three columns
+                    // of its channel group before writing any, so in-place reuse of an
+                    // old column is safe (no other thread touches that channel group)
+                    const int64_t total4 = a.C / 4, per = (total4 + parts - 1) / parts;
+                    const int64_t lo = (2 * int64_t(q.h) + q.half) * per, hi = min(total4, lo + per);
+                    const int32_t *ref = a.wref + (int64_t(q.n0) + q.acc) * 3;
+                    const int r0 = ref[0], r1 = ref[1], r2 = ref[2];
+                    auto col = [&](int r, int64_t i) -> float4 {
+                        return r >= 0 ? __ldg(reinterpret_cast<const float4 *>(a.x + int64_t(r) * a.x_stride) + i)
+                                      : hdst[(-1 - r) * (a.C / 4) + i];
+                    };
+                    for (int64_t i = lo + lane; i < hi; i += 32) {
+                        const float4 v0 = col(r0, i), v1 = col(r1, i), v2 = col(r2, i);
+                        hdst[i] = v0;
+                        hdst[a.C / 4 + i] = v1;
+                        hdst[2 * (a.C / 4) + i] = v2;
+                    }
+                }
+            }
+            u = next_unit<kStages>(sc, a, units, p, lane);
+            if (u >= 0) q = walk_path(a, u, lane);
+        }
+        // the end marker, in the stage the consumers take after the last unit: the
+        // committing units were all scanned, so every producer knows their count
+        // (after a status that is not zero, stage 0 ends everything)
+        if (ok && (failed ? p == 0 : sc.live % kStages == p)) {
+            if (__all_sync(all, ph == 0 || wait_or_abort(empty + p, uint32_t((ph - 1) & 1), abort_flag))) {
+                if (lane == 0) {
+                    sa[SM_M] = -1;
+                    gdn::mbar_arrive_expect_tx(fb, 0);
+                }
+                ++ph;
+            }
+        }
+        // copies still in flight (after a timeout) land before the CTA exits
+        if (ph > 0 && lane == 0) gdn::mbar_wait_bounded(fb, uint32_t((ph - 1) & 1));
+    } else {
+        // ---- consumers: warp w owns rows 4 w .. 4 w + 3 of each unit ------------
+        const int r0 = 4 * warp;
+        uint32_t pbits = 0;  // parity of the next phase, per stage
+        for (int j = 0;; ++j) {
+            const int st = j % kStages;
+            if (!__all_sync(all, wait_or_abort(full + st, (pbits >> st) & 1u, abort_flag))) break;
+            const int *sa = small + st * SM_WORDS;
+            const float *sf = reinterpret_cast<const float *>(sa);
+            const int m = sa[SM_M];
+            if (m < 0) break;  // no more units
+            const float gam = sf[SM_GAM];
+            const int slot = sa[SM_SLOT], hh = sa[SM_HH];
+            const unsigned char *stage = smem_raw + size_t(st) * kStageBytes;
+            const float *tile = reinterpret_cast<const float *>(stage);
+            const float *ent = reinterpret_cast<const float *>(stage + kTileBytes);
+            float4 sv[4];
+            if (m) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    sv[r] = *reinterpret_cast<const float4 *>(tile + (r0 + r) * D + 4 * lane);
+                    sv[r].x *= gam; sv[r].y *= gam; sv[r].z *= gam; sv[r].w *= gam;
+                }
+            }
+            const int nb = m ? (m + kEntries - 1) / kEntries : 1;
+            bool ok = true;
+            for (int b = 0; b < nb; ++b) {
+                if (b > 0 && !__all_sync(all, wait_or_abort(full + st, (pbits >> st) & 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const int cnt = m ? batch_count<kEntries>(m, b) : 0;
+                // root first: staging slot e holds leaf-first entry m - 1 - kEntries b - e
+                for (int e = 0; e < cnt; ++e) {
+                    const float cj = sf[SM_COEF + m - 1 - kEntries * b - e];
+                    const float *en = ent + e * kEntryFloats;
+                    const float4 kv = *reinterpret_cast<const float4 *>(en + 4 * lane);
+                    const float4 uv = *reinterpret_cast<const float4 *>(en + D + r0);
+                    const float uu[4] = {uv.x * cj, uv.y * cj, uv.z * cj, uv.w * cj};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        sv[r].x = fmaf(uu[r], kv.x, sv[r].x);
+                        sv[r].y = fmaf(uu[r], kv.y, sv[r].y);
+                        sv[r].z = fmaf(uu[r], kv.z, sv[r].z);
+                        sv[r].w = fmaf(uu[r], kv.w, sv[r].w);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) arrive(empty + st);  // this warp's reads of the phase are done
+                pbits ^= 1u << st;
+            }
+            if (!ok) break;
+            if (!m) continue;
+            float *dst = a.ssm + ((int64_t(slot) * a.Hv + (hh >> 1)) * D + kUnitRows * (hh & 1) + r0) * D + 4 * lane;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) *reinterpret_cast<float4 *>(dst + r * D) = sv[r];
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *abort_flag) gdn::record_status(a.status, GDN_DEV_TIMEOUT);
+}
+
+// One persistent CTA per SM (or per unit, when there are fewer).
+template <class R>
+int launch_stream(const CommitArgs &a, int64_t units, cudaStream_t st) {
+    auto k = commit_stream_kernel<R>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(R::BYTES)) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    const int sms = gdn::sm_count_current();
+    if (sms <= 0) return GDN_ERR_LAUNCH;
+    const unsigned grid = unsigned(std::min<int64_t>(units, sms));
+    return gdn::launch_pdl(k, dim3(grid), dim3(R::kThreads), R::BYTES, st, a) == cudaSuccess ? GDN_OK
+                                                                                         : GDN_ERR_LAUNCH;
+}
+
 int commit_entry(const gdn_dims *dims, const int32_t *accepted, const int32_t *parents, const int32_t *node_off,
                  const int32_t *slot_map, const float *replay, int64_t replay_stride, const float *win,
                  const float *x, int64_t x_stride, const int32_t *wref, float *ssm, float *conv_hist,
@@ -303,6 +674,9 @@ int commit_entry(const gdn_dims *dims, const int32_t *accepted, const int32_t *p
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (gdn::launch_pdl(commit_preflight_kernel, dim3(unsigned((S + 7) / 8)), dim3(256), 0, st, a) != cudaSuccess)
         return GDN_ERR_LAUNCH;
+    if (D == cst::D)
+        return dims->max_seq_nodes <= cst::RingShort::kEntries ? launch_stream<cst::RingShort>(a, S * Hv * 2, st)
+                                                                : launch_stream<cst::RingLong>(a, S * Hv * 2, st);
     // CTAs of 32 state rows: d / 32 per head (one for d = 16)
     const unsigned cph = unsigned((D + kCtaRows - 1) / kCtaRows);
     const dim3 grid{unsigned(Hv) * cph, unsigned(S)};
