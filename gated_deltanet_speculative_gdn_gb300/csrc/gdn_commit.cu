@@ -275,8 +275,9 @@ __global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const
 // state).  The tile and the path's replay rows (k^_j and the unit's half of
 // u_j) arrive by bulk copies into a ring of kStages stages, so each SM keeps
 // well over 100 KB of state in flight while it applies earlier units.  A stage
-// holds kEntries path entries; a longer path passes through in batches, each
-// batch one more phase of the stage's barriers.
+// holds the tile and kEntries path entries; the entries of a longer path past
+// those go into the tile's own space once the consumers hold the tile in
+// registers (a second phase of the stage's full barrier).
 //
 // Producer warp p fills stage p for every kStages-th committing unit.  It finds
 // its units with a warp-wide scan of `accepted` (one lane per unit, a ballot),
@@ -291,13 +292,15 @@ __global__ void __launch_bounds__(kApplyWarps * 32, 6) commit_apply_kernel(const
 // Sixteen consumer warps take the stages in ring order and learn everything
 // from the stage itself: warp w owns rows 4 w .. 4 w + 3 of the unit (lane l:
 // float4 column group l), loads them times Gamma, adds the path's rank-1 terms
-// root first and stores them with coalesced 128-bit stores.
+// root first (packed pairs of fp32 multiply-adds) and stores them with
+// coalesced 128-bit stores.
 namespace cst {
 constexpr int D = 128;
 constexpr int kUnitRows = 64;                   // state rows per unit
 constexpr int kEntryFloats = D + kUnitRows;     // k^_j | the unit's 64 entries of u_j
 constexpr uint32_t kTileBytes = kUnitRows * D * 4;
 constexpr uint32_t kEntryBytes = kEntryFloats * 4;
+constexpr int kTileEntries = kTileBytes / kEntryBytes;  // second-phase entries the tile's space holds
 constexpr int kConsumerWarps = kUnitRows / 4;
 // per-stage small area (4-byte words)
 constexpr int SM_M = 0;                         // path length; 0: nothing to apply; -1: no more units
@@ -310,22 +313,26 @@ constexpr int SM_WORDS = SM_NODE + gdn::kMaxSeqNodes;
 
 // The ring: kStages stages (= producer warps) of one tile and kEntries path
 // entries each.  Five stages of 16 entries when no path is longer than 16
-// (trees of up to 16 nodes); four of 32 otherwise, so that long paths (chains)
-// pass in fewer batches.
+// (trees of up to 16 nodes); four of 32 otherwise, so that a path of up to 64
+// entries passes in two phases.  Barriers per stage: full (the copies landed;
+// one or two phases per unit), tread (every consumer warp holds the tile) and
+// empty (every consumer warp is done with the stage), one phase each per unit.
 template <int kStages_, int kEntries_>
 struct Ring {
     static constexpr int kStages = kStages_, kEntries = kEntries_;
     static constexpr uint32_t kStageBytes = kTileBytes + kEntries * kEntryBytes;
     static constexpr int kThreads = 32 * (kConsumerWarps + kStages);
+    static constexpr int kMaxPath = kEntries + kTileEntries;
     static constexpr size_t SMALL_OFF = size_t(kStages) * kStageBytes;
     static constexpr size_t BAR_OFF = SMALL_OFF + size_t(kStages) * SM_WORDS * 4;
-    static constexpr size_t BYTES = BAR_OFF + 2 * kStages * 8 + 16;
+    static constexpr size_t BYTES = BAR_OFF + 3 * kStages * 8 + 16;
     static_assert(BYTES <= 227 * 1024, "shared memory");
     static_assert(kStageBytes % 16 == 0 && kEntryBytes % 16 == 0 && BAR_OFF % 8 == 0, "16-byte copies");
-    static_assert(kEntries <= 32, "one lane per staged entry");
+    static_assert(kEntries <= 32 && kTileEntries <= 64, "one lane per copied entry");
 };
 using RingShort = Ring<5, 16>;
 using RingLong = Ring<4, 32>;
+static_assert(RingLong::kMaxPath >= gdn::kMaxSeqNodes, "any path in two phases");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (*abort_flag) return false;
@@ -336,10 +343,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 __device__ __forceinline__ void arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gdn::smem_addr(bar)) : "memory");
 }
-// entries of batch b of a path of m: root first, leaf-first indices
-// m - 1 - kEntries b down to m - kEntries (b + 1), staging slots 0, 1, ...
-template <int kEntries>
-__device__ __forceinline__ int batch_count(int m, int b) { return min(kEntries, m - kEntries * b); }
+__device__ __forceinline__ uint64_t pair_of(float x) { return gdn::f2pack(x, x); }
 
 // A producer's view of its units: the CTA's units u = blockIdx.x + k gridDim.x
 // are scanned 32 at a time; committing units are numbered in order, and
@@ -376,7 +380,7 @@ struct Path {
     int s, h, half, acc, n0, slot, m, node_lo, node_hi;
     bool bad;
 };
-__device__ __forceinline__ Path walk_path(const CommitArgs &a, int64_t u, int lane) {
+__device__ __forceinline__ Path walk_path(const CommitArgs &a, int64_t u, int lane, int max_path) {
     Path q;
     q.s = int(u / (2 * a.Hv));
     q.h = int((u >> 1) % a.Hv);
@@ -403,7 +407,7 @@ __device__ __forceinline__ Path walk_path(const CommitArgs &a, int64_t u, int la
             cur = nx;
         }
     }
-    if (q.bad) q.m = 0;
+    if (q.bad || q.m > max_path) q.m = 0;  // (paths are at most max_seq_nodes long)
     return q;
 }
 }  // namespace cst
@@ -417,8 +421,9 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
     extern __shared__ __align__(16) unsigned char smem_raw[];
     int *small = reinterpret_cast<int *>(smem_raw + SMALL_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + BAR_OFF);
-    uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<int *>(full + 2 * kStages);  // [1]: the status was not zero
+    uint64_t *tread = full + kStages;
+    uint64_t *empty = tread + kStages;
+    volatile int *abort_flag = reinterpret_cast<int *>(full + 3 * kStages);  // [1]: the status was not zero
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned all = 0xffffffffu;
     const int64_t units = int64_t(a.S) * a.Hv * 2;
@@ -428,6 +433,7 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             gdn::mbar_init(full + i, 1);
+            gdn::mbar_init(tread + i, kConsumerWarps);
             gdn::mbar_init(empty + i, kConsumerWarps);
         }
         gdn::fence_mbar_init();
@@ -443,11 +449,12 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
         float *sf = reinterpret_cast<float *>(sa);
         unsigned char *stage = smem_raw + size_t(p) * kStageBytes;
         float *ent = reinterpret_cast<float *>(stage + kTileBytes);
+        float *ent2 = reinterpret_cast<float *>(stage);  // second phase: the tile's space
         UnitScan sc;
-        int ph = 0;  // phases of stage p issued
+        int nu = 0, fph = 0;  // units issued into stage p, phases of its full barrier
         bool ok = true;
         int64_t u = next_unit<kStages>(sc, a, units, p, lane);
-        Path q = walk_path(a, u >= 0 ? u : 0, lane);  // before the wait: index inputs only
+        Path q = walk_path(a, u >= 0 ? u : 0, lane, R::kMaxPath);  // before the wait: index inputs only
         gdn::grid_dep_wait();  // status, the state pool, the replay rows and the windows
         // one reading of the status for the whole CTA: not zero, nothing is committed
         if (p == 0 && lane == 0) abort_flag[1] = *reinterpret_cast<volatile int32_t *>(a.status) != 0;
@@ -477,47 +484,43 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
             c_hi *= tot_lo;
             const float gam = tot_lo * __shfl_sync(all, x_hi, 31);
             const int m = q.m;
-            const int nb = m ? (m + kEntries - 1) / kEntries : 1;
-            for (int b = 0; b < nb; ++b) {
-                // the stage's previous phase has been read by every consumer warp
-                if (!__all_sync(all, ph == 0 || wait_or_abort(empty + p, uint32_t((ph - 1) & 1), abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                ++ph;
-                if (b == 0) {
-                    if (lane < m) {
-                        sa[SM_COEF + lane] = __float_as_int(c_lo);
-                        sa[SM_NODE + lane] = q.node_lo;
-                    }
-                    if (lane + 32 < m) {
-                        sa[SM_COEF + lane + 32] = __float_as_int(c_hi);
-                        sa[SM_NODE + lane + 32] = q.node_hi;
-                    }
-                    if (lane == 0) {
-                        sa[SM_M] = m;
-                        sf[SM_GAM] = gam;
-                        sa[SM_SLOT] = q.slot;
-                        sa[SM_HH] = 2 * q.h + q.half;
-                    }
-                    __threadfence_block();
-                }
-                __syncwarp();
-                const int cnt = m ? batch_count<kEntries>(m, b) : 0;
-                if (lane == 0)
-                    gdn::mbar_arrive_expect_tx(fb, (b == 0 && m ? kTileBytes : 0) + cnt * kEntryBytes);
-                __syncwarp();
-                if (b == 0 && m && lane == 0)
-                    gdn::bulk_load(stage, a.ssm + ((int64_t(q.slot) * a.Hv + q.h) * D + kUnitRows * q.half) * D,
-                                   kTileBytes, fb);
-                if (lane < cnt) {
-                    const float *rr = row0 + sa[SM_NODE + m - 1 - kEntries * b - lane] * rnode;
-                    float *dst = ent + lane * kEntryFloats;
-                    gdn::bulk_load(dst, rr, D * 4, fb);
-                    gdn::bulk_load(dst + D, rr + D + kUnitRows * q.half, kUnitRows * 4, fb);
-                }
+            // the stage's previous unit is done with
+            if (!__all_sync(all, nu == 0 || wait_or_abort(empty + p, uint32_t((nu - 1) & 1), abort_flag))) {
+                ok = false;
+                break;
             }
-            if (ok && m) {
+            ++nu;
+            if (lane < m) {
+                sa[SM_COEF + lane] = __float_as_int(c_lo);
+                sa[SM_NODE + lane] = q.node_lo;
+            }
+            if (lane + 32 < m) {
+                sa[SM_COEF + lane + 32] = __float_as_int(c_hi);
+                sa[SM_NODE + lane + 32] = q.node_hi;
+            }
+            if (lane == 0) {
+                sa[SM_M] = m;
+                sf[SM_GAM] = gam;
+                sa[SM_SLOT] = q.slot;
+                sa[SM_HH] = 2 * q.h + q.half;
+            }
+            __threadfence_block();
+            __syncwarp();
+            // phase 1: the tile and the first kEntries entries, root first
+            const int cnt = min(m, kEntries), cnt2 = m - cnt;
+            if (lane == 0) gdn::mbar_arrive_expect_tx(fb, m ? kTileBytes + cnt * kEntryBytes : 0);
+            ++fph;
+            __syncwarp();
+            if (m && lane == 0)
+                gdn::bulk_load(stage, a.ssm + ((int64_t(q.slot) * a.Hv + q.h) * D + kUnitRows * q.half) * D,
+                               kTileBytes, fb);
+            if (lane < cnt) {
+                const float *rr = row0 + sa[SM_NODE + m - 1 - lane] * rnode;
+                float *dst = ent + lane * kEntryFloats;
+                gdn::bulk_load(dst, rr, D * 4, fb);
+                gdn::bulk_load(dst + D, rr + D + kUnitRows * q.half, kUnitRows * 4, fb);
+            }
+            if (m) {
                 // this unit's share of the history copy, conv_hist[slot] <- window of the accepted node
                 const int64_t parts = int64_t(a.Hv) * 2;
                 float4 *hdst = reinterpret_cast<float4 *>(a.hist + int64_t(q.slot) * 3 * a.C);
@@ -548,30 +551,48 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
                     }
                 }
             }
+            if (cnt2 > 0) {
+                // phase 2: the remaining entries into the tile's space, once every
+                // consumer warp holds the tile
+                if (!__all_sync(all, wait_or_abort(tread + p, uint32_t((nu - 1) & 1), abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) gdn::mbar_arrive_expect_tx(fb, cnt2 * kEntryBytes);
+                ++fph;
+                __syncwarp();
+                for (int e = lane; e < cnt2; e += 32) {
+                    const float *rr = row0 + sa[SM_NODE + m - 1 - kEntries - e] * rnode;
+                    float *dst = ent2 + e * kEntryFloats;
+                    gdn::bulk_load(dst, rr, D * 4, fb);
+                    gdn::bulk_load(dst + D, rr + D + kUnitRows * q.half, kUnitRows * 4, fb);
+                }
+            }
             u = next_unit<kStages>(sc, a, units, p, lane);
-            if (u >= 0) q = walk_path(a, u, lane);
+            if (u >= 0) q = walk_path(a, u, lane, R::kMaxPath);
         }
         // the end marker, in the stage the consumers take after the last unit: the
         // committing units were all scanned, so every producer knows their count
         // (after a status that is not zero, stage 0 ends everything)
         if (ok && (failed ? p == 0 : sc.live % kStages == p)) {
-            if (__all_sync(all, ph == 0 || wait_or_abort(empty + p, uint32_t((ph - 1) & 1), abort_flag))) {
+            if (__all_sync(all, nu == 0 || wait_or_abort(empty + p, uint32_t((nu - 1) & 1), abort_flag))) {
                 if (lane == 0) {
                     sa[SM_M] = -1;
                     gdn::mbar_arrive_expect_tx(fb, 0);
                 }
-                ++ph;
+                ++fph;
             }
         }
         // copies still in flight (after a timeout) land before the CTA exits
-        if (ph > 0 && lane == 0) gdn::mbar_wait_bounded(fb, uint32_t((ph - 1) & 1));
+        if (fph > 0 && lane == 0) gdn::mbar_wait_bounded(fb, uint32_t((fph - 1) & 1));
     } else {
         // ---- consumers: warp w owns rows 4 w .. 4 w + 3 of each unit ------------
         const int r0 = 4 * warp;
-        uint32_t pbits = 0;  // parity of the next phase, per stage
+        uint32_t pbits = 0;  // parity of the next phase of each stage's full barrier
         for (int j = 0;; ++j) {
             const int st = j % kStages;
             if (!__all_sync(all, wait_or_abort(full + st, (pbits >> st) & 1u, abort_flag))) break;
+            pbits ^= 1u << st;
             const int *sa = small + st * SM_WORDS;
             const float *sf = reinterpret_cast<const float *>(sa);
             const int m = sa[SM_M];
@@ -579,48 +600,50 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
             const float gam = sf[SM_GAM];
             const int slot = sa[SM_SLOT], hh = sa[SM_HH];
             const unsigned char *stage = smem_raw + size_t(st) * kStageBytes;
-            const float *tile = reinterpret_cast<const float *>(stage);
-            const float *ent = reinterpret_cast<const float *>(stage + kTileBytes);
-            float4 sv[4];
+            // rows as pairs of fp32: (x, y) and (z, w) of each row
+            uint64_t sp[4][2];
             if (m) {
+                const uint64_t gg = pair_of(gam);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    sv[r] = *reinterpret_cast<const float4 *>(tile + (r0 + r) * D + 4 * lane);
-                    sv[r].x *= gam; sv[r].y *= gam; sv[r].z *= gam; sv[r].w *= gam;
+                    const ulonglong2 t =
+                        *reinterpret_cast<const ulonglong2 *>(stage + ((r0 + r) * D + 4 * lane) * 4);
+                    sp[r][0] = gdn::mul2(t.x, gg);
+                    sp[r][1] = gdn::mul2(t.y, gg);
                 }
             }
-            const int nb = m ? (m + kEntries - 1) / kEntries : 1;
-            bool ok = true;
-            for (int b = 0; b < nb; ++b) {
-                if (b > 0 && !__all_sync(all, wait_or_abort(full + st, (pbits >> st) & 1u, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                const int cnt = m ? batch_count<kEntries>(m, b) : 0;
-                // root first: staging slot e holds leaf-first entry m - 1 - kEntries b - e
-                for (int e = 0; e < cnt; ++e) {
-                    const float cj = sf[SM_COEF + m - 1 - kEntries * b - e];
-                    const float *en = ent + e * kEntryFloats;
-                    const float4 kv = *reinterpret_cast<const float4 *>(en + 4 * lane);
-                    const float4 uv = *reinterpret_cast<const float4 *>(en + D + r0);
-                    const float uu[4] = {uv.x * cj, uv.y * cj, uv.z * cj, uv.w * cj};
+            __syncwarp();
+            if (lane == 0) arrive(tread + st);  // this warp holds its rows of the tile
+            // root first: slot e of phase 1 holds leaf-first entry m - 1 - e, slot e
+            // of phase 2 (in the tile's space) entry m - 1 - kEntries - e
+            const int cnt = min(m, kEntries), cnt2 = m - cnt;
+            auto apply = [&](const float *en, float cj) {
+                const ulonglong2 kv = *reinterpret_cast<const ulonglong2 *>(en + 4 * lane);
+                const float4 uv = *reinterpret_cast<const float4 *>(en + D + r0);
+                const float uu[4] = {uv.x * cj, uv.y * cj, uv.z * cj, uv.w * cj};
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        sv[r].x = fmaf(uu[r], kv.x, sv[r].x);
-                        sv[r].y = fmaf(uu[r], kv.y, sv[r].y);
-                        sv[r].z = fmaf(uu[r], kv.z, sv[r].z);
-                        sv[r].w = fmaf(uu[r], kv.w, sv[r].w);
-                    }
+                for (int r = 0; r < 4; ++r) {
+                    const uint64_t ur = pair_of(uu[r]);
+                    sp[r][0] = gdn::fma2(ur, kv.x, sp[r][0]);
+                    sp[r][1] = gdn::fma2(ur, kv.y, sp[r][1]);
                 }
-                __syncwarp();
-                if (lane == 0) arrive(empty + st);  // this warp's reads of the phase are done
+            };
+            const float *ent = reinterpret_cast<const float *>(stage + kTileBytes);
+            for (int e = 0; e < cnt; ++e) apply(ent + e * kEntryFloats, sf[SM_COEF + m - 1 - e]);
+            if (cnt2 > 0) {
+                if (!__all_sync(all, wait_or_abort(full + st, (pbits >> st) & 1u, abort_flag))) break;
                 pbits ^= 1u << st;
+                const float *ent2 = reinterpret_cast<const float *>(stage);
+                for (int e = 0; e < cnt2; ++e)
+                    apply(ent2 + e * kEntryFloats, sf[SM_COEF + m - 1 - kEntries - e]);
             }
-            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) arrive(empty + st);  // this warp is done with the stage
             if (!m) continue;
             float *dst = a.ssm + ((int64_t(slot) * a.Hv + (hh >> 1)) * D + kUnitRows * (hh & 1) + r0) * D + 4 * lane;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) *reinterpret_cast<float4 *>(dst + r * D) = sv[r];
+            for (int r = 0; r < 4; ++r)
+                *reinterpret_cast<ulonglong2 *>(dst + r * D) = make_ulonglong2(sp[r][0], sp[r][1]);
         }
     }
     __syncthreads();
