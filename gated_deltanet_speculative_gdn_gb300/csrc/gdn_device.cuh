@@ -129,20 +129,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, i
                  : "memory");
 }
 
-// 3-D TMA tile store shared -> global (bulk-group completion).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until this thread's committed bulk stores have read their shared-memory
-// sources (the buffers may be rewritten) / have completed.
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16),
 // completing on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

@@ -447,25 +447,25 @@ __global__ void __launch_bounds__(kThreads, (NMAX > kSeg ? 1 : 2))
 // deep ring of S0 slots.
 //
 // One CTA per SM walks a list of items.  Warp roles:
-//   warp 0       TMA producer: S0 of each item as four 16 KB K-chunks
-//                ([128 rows][32 floats], 128-byte swizzle = the tensor cores'
-//                K-major operand layout) into a ring of NR slots;
+//   warp 0       TMA producer, items in order: the item's q/k rows into B
+//                buffer v % NB (same layout as the chunks) once the item NB
+//                before it is done with that buffer, then S0 as four 16 KB
+//                K-chunks ([128 rows][32 floats], 128-byte swizzle = the
+//                tensor cores' K-major operand layout) into a ring of NR slots;
 //   warps 1-3    MMA issuers, items and chunks in order: the Gram terms once
 //                the item's B is split (warp 1); A_hi [B_hi | B_lo] once a
 //                chunk lands (warp 2); A_lo [B_hi | B_lo] once the chunk holds
 //                its lo part, which frees the slot (warp 3);
-//   warps 4-7    team 0 and warps 8-11 team 1, on alternate items: the item's
-//                q/k rows by TMA into the team's B buffer (same layout as the
-//                chunks), gates, the ancestor decays, norms and path
-//                coefficients from the Gram terms, T, and the per-row epilogue
-//                reading the accumulators from tensor memory (thread i owns
-//                state row i);
+//   warps 4-7    team 0 and warps 8-11 team 1, on alternate items: gates, the
+//                ancestor decays, norms and path coefficients from the Gram
+//                terms, T, and the per-row epilogue reading the accumulators
+//                from tensor memory (thread i owns state row i);
 //   warps 12-15  splitters, items in order: B's lo rows as soon as the item's
 //                q/k rows land, then the lo part of every S0 chunk, in place,
 //                as soon as its A_hi products are done.
-// A team's next q/k rows land while it runs the current epilogue, and the S0
-// ring runs ahead of both teams, so loads, tensor-core work and CUDA-core
-// work of different items overlap.
+// With three B buffers for two teams, an item's q/k rows land while the
+// previous items still use theirs, and the S0 ring runs ahead of both teams,
+// so loads, tensor-core work and CUDA-core work of different items overlap.
 namespace wsv {
 constexpr int D = 128;
 constexpr int kWarps = 16;
@@ -478,13 +478,14 @@ constexpr int NR = 6;                              // S0 ring depth (K-chunks)
 constexpr int kPrefetch = 2;                       // items whose state is requested into L2 ahead
 constexpr uint32_t kChunk = 128 * 128;             // one S0 K-chunk: 128 rows x 32 fp32
 constexpr uint32_t kBChunk = 64 * 128;             // one B K-chunk: rows 0-15 k, 16-31 q, 32-63 their lo
-constexpr uint32_t kBTeam = 4 * kBChunk;           // one team's B
+constexpr uint32_t kBTeam = 4 * kBChunk;           // one item's B
+constexpr int NB = 3;                              // B buffers, item v in buffer v % NB
 constexpr uint32_t kQKBox = 16 * 128;              // 16 rows of k or q, one K-chunk
 constexpr uint32_t RAW = 0;
 constexpr uint32_t BT = RAW + NR * kChunk;         // per team
-constexpr uint32_t kStage = 16 * D * 4;            // one [16 nodes][d] output tile
-constexpr uint32_t STG = BT + 2 * kBTeam;          // per team: o | k^ | u tiles for TMA stores
-constexpr uint32_t SMALL = STG + 2 * 3 * kStage;
+constexpr uint32_t kStage = 16 * D * 4;            // one [16 nodes][d] tile
+constexpr uint32_t VT = BT + NB * kBTeam;          // per team: the item's v rows
+constexpr uint32_t SMALL = VT + 2 * kStage;
 // per-team small area (4-byte words), [16][16] matrices:
 //   KA + KB = k_t . k_j and QA + QB = q_t . k_j (Gram partial sums from the
 //   hi and lo rows, row t); GM = gamma_{j->t} (row t; 1 on the diagonal, 0
@@ -500,9 +501,11 @@ constexpr int B_RFULL = 0;                 // NR: S0 chunk landed
 constexpr int B_HDONE = B_RFULL + NR;      // NR: the chunk's A_hi products done (1)
 constexpr int B_LFULL = B_HDONE + NR;      // NR: its lo part written in place (64)
 constexpr int B_REMPTY = B_LFULL + NR;     // NR: the lo part's products done, slot free (1)
-constexpr int B_QFULL = B_REMPTY + NR;     // per team: q/k rows landed (1 + bytes)
-constexpr int B_BREADY = B_QFULL + 2;      // per team: B's lo rows written (128)
-constexpr int B_GFULL = B_BREADY + 2;      // per team: Gram terms complete (1)
+constexpr int B_QFULL = B_REMPTY + NR;     // per B buffer: q/k rows landed (1 + bytes)
+constexpr int B_BREADY = B_QFULL + NB;     // per B buffer: its lo rows written (128)
+constexpr int B_BFREE = B_BREADY + NB;     // per B buffer: the item is done with it (1 from each
+                                           // product issuer, 1 from the team)
+constexpr int B_GFULL = B_BFREE + NB;      // per team: Gram terms complete (1)
 constexpr int B_ACCFULL = B_GFULL + 2;     // per team: accumulators complete (1 from each product issuer)
 constexpr int B_ACCEMPTY = B_ACCFULL + 2;  // per team: accumulators read (128)
 constexpr int B_VFULL = B_ACCEMPTY + 2;    // per team: the item's v rows landed in its u tile (1 + bytes)
@@ -558,9 +561,7 @@ __device__ __forceinline__ float4 lo4(float4 x) {
 
 __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
     tree_verify_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap xmap,
-                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-                          const __grid_constant__ CUtensorMap rmap,
-                          const VerifyArgs a) {
+                          const __grid_constant__ CUtensorMap vmap, const VerifyArgs a) {
     using namespace wsv;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sb =
@@ -611,7 +612,8 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t count = 1;
             if (i >= B_LFULL && i < B_LFULL + NR) count = kSplitThreads;
-            if (i >= B_BREADY && i < B_BREADY + 2) count = 128;
+            if (i >= B_BREADY && i < B_BREADY + NB) count = 128;
+            if (i >= B_BFREE && i < B_BFREE + NB) count = 4;
             if (i >= B_ACCEMPTY && i < B_ACCEMPTY + 2) count = 128;
             if (i >= B_ACCFULL && i < B_ACCFULL + 2) count = 2;
             if (i == B_DRAIN) count = 3;
@@ -649,12 +651,29 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) gdn::tma_prefetch_2d(&tmap, 32 * c, (e.w * a.Hv + e.x % a.Hv) * D);
             };
-            int g = 0;
+            int g = 0, qk_issued = 0;
             for (; g < nchunks; ++g) {
                 const int r = g % NR;
-                if (g >= NR && !wait_or_abort(bars + B_REMPTY + r, uint32_t((g / NR - 1) & 1), abort_flag)) break;
-                if ((g & 3) == 0) prefetch_item((g >> 2) + kPrefetch + 1);
                 const int4 e = list[g >> 2];
+                if ((g & 3) == 0) {
+                    // the item's q/k rows into its B buffer, once the item NB
+                    // before has finished with it (its products and its team)
+                    const int v = g >> 2, b = v % NB;
+                    if (v >= NB && !wait_or_abort(bars + B_BFREE + b, uint32_t((v / NB - 1) & 1), abort_flag))
+                        break;
+                    const int kh = (e.x % a.Hv) / (a.Hv / a.Hk);
+                    unsigned char *bt = sb + BT + b * kBTeam;
+                    uint64_t *qbar = bars + B_QFULL + b;
+                    gdn::mbar_arrive_expect_tx(qbar, 8 * kQKBox);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        gdn::tma_load_2d(bt + c * kBChunk, &xmap, a.Hk * D + kh * D + 32 * c, e.y, qbar);
+                        gdn::tma_load_2d(bt + c * kBChunk + kQKBox, &xmap, kh * D + 32 * c, e.y, qbar);
+                    }
+                    ++qk_issued;
+                    prefetch_item(v + kPrefetch + 1);
+                }
+                if (g >= NR && !wait_or_abort(bars + B_REMPTY + r, uint32_t((g / NR - 1) & 1), abort_flag)) break;
                 uint64_t *fb = bars + B_RFULL + r;
                 gdn::mbar_arrive_expect_tx(fb, kChunk);
                 gdn::tma_load_2d(sb + RAW + r * kChunk, &tmap, 32 * (g & 3), (e.w * a.Hv + e.x % a.Hv) * D, fb);
@@ -664,6 +683,11 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 for (int r = 0; r < NR; ++r) {
                     const int last = g - 1 - ((g - 1 - r) % NR + NR) % NR;  // last chunk issued into slot r
                     if (g > 0 && last >= 0) gdn::mbar_wait_bounded(bars + B_RFULL + r, uint32_t((last / NR) & 1));
+                }
+                for (int b = 0; b < NB; ++b) {
+                    const int last = qk_issued - 1 - ((qk_issued - 1 - b) % NB + NB) % NB;  // last item in buffer b
+                    if (qk_issued > 0 && last >= 0)
+                        gdn::mbar_wait_bounded(bars + B_QFULL + b, uint32_t((last / NB) & 1));
                 }
             }
         }
@@ -676,12 +700,12 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         if (lane == 0) {
             bool ok = true;
             for (int v = 0; v < nv && ok; ++v) {
-                const int t = v & 1, ut = v >> 1;
-                if (!wait_or_abort(bars + B_BREADY + t, uint32_t(ut & 1), abort_flag)) break;
+                const int t = v & 1, ut = v >> 1, b = v % NB;
+                if (!wait_or_abort(bars + B_BREADY + b, uint32_t((v / NB) & 1), abort_flag)) break;
                 if (ut > 0 && !wait_or_abort(bars + B_ACCEMPTY + t, uint32_t((ut - 1) & 1), abort_flag)) break;
                 gdn::tc_fence_after_sync();
                 const uint32_t dacc = tmem + TEAM_COLS * t;
-                const uint32_t bt0 = sbase + BT + t * kBTeam;
+                const uint32_t bt0 = sbase + BT + b * kBTeam;
                 if (warp == kIssueGram) {
                     // Gram terms of B's 64 rows [k | q | k_lo | q_lo] with themselves
                     for (int kt = 0; kt < 4; ++kt) {
@@ -692,6 +716,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                             gdn::mma_tf32(dacc + GCOL, gd, gd, IDESC_GRAM, (kt | ks) != 0);
                     }
                     gdn::mma_commit(bars + B_GFULL + t);
+                    gdn::mma_commit(bars + B_BFREE + b);
                     continue;
                 }
                 for (int kb = 0; kb < 4; ++kb) {
@@ -726,7 +751,10 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                         gdn::mma_commit(bars + B_REMPTY + r);
                     }
                 }
-                if (ok) gdn::mma_commit(bars + B_ACCFULL + t);
+                if (ok) {
+                    gdn::mma_commit(bars + B_ACCFULL + t);
+                    gdn::mma_commit(bars + B_BFREE + b);
+                }
             }
             // every tensor-core operation of these threads completes before the
             // tensor memory is released
@@ -744,9 +772,9 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         for (int g = 0; g < nchunks; ++g) {
             const int r = g % NR;
             if ((g & 3) == 0) {
-                const int v = g >> 2, t = v & 1;
-                if (!wait_or_abort(bars + B_QFULL + t, uint32_t((v >> 1) & 1), abort_flag)) break;
-                unsigned char *bt = sb + BT + t * kBTeam;
+                const int v = g >> 2, b = v % NB;
+                if (!wait_or_abort(bars + B_QFULL + b, uint32_t((v / NB) & 1), abort_flag)) break;
+                unsigned char *bt = sb + BT + b * kBTeam;
 #pragma unroll
                 for (int j = 0; j < (4 * 32 * 8) / kSplitThreads; ++j) {
                     const int idx = st + kSplitThreads * j;  // 16-byte unit: K-chunk idx / 256, rows 0-31
@@ -755,7 +783,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                     *reinterpret_cast<float4 *>(p + 32 * 128) = lo4(x);
                 }
                 gdn::fence_proxy_async_smem();
-                mbar_arrive(bars + B_BREADY + t);
+                mbar_arrive(bars + B_BREADY + b);
             }
             if (!wait_or_abort(bars + B_HDONE + r, uint32_t((g / NR) & 1), abort_flag)) break;
             float4 *c = reinterpret_cast<float4 *>(sb + RAW + r * kChunk);
@@ -782,10 +810,8 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
         float *qqa = tws + T_QQA, *qqb = tws + T_QQB, *beta_s = tws + T_BETA, *dec_s = tws + T_DEC;
         float *gsk = tws + T_GSK, *gsq = tws + T_GSQ, *rk_s = tws + T_RK, *gam_s = tws + T_GAM;
         int *par = reinterpret_cast<int *>(tws + T_PAR);
-        unsigned char *bt_t = sb + BT + team * kBTeam;
-        // output tiles of a full (16-node) item, written by TMA stores
-        float *stg_o = reinterpret_cast<float *>(sb + STG + team * 3 * kStage);
-        float *stg_k = stg_o + kSeg * D, *stg_u = stg_k + kSeg * D;
+        // the item's v rows (TMA), read by the epilogue
+        float *stg_v = reinterpret_cast<float *>(sb + VT + team * kStage);
 
         // parents and gate inputs of the team's next item, loaded one item ahead
         int p_nx = -1;
@@ -804,26 +830,11 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             }
         };
         prefetch(team);
-        // one thread of the team loads an item's raw q/k rows into the team's B
-        // and its v rows into the team's v tile (rows n0 .. n0 + 15; rows past
-        // the sequence's last node belong to the next sequence, or are
-        // zero-filled past the tensor: they only feed outputs that are never
-        // written)
-        int qk_issued = 0, v_issued = 0;
-        auto issue_qk = [&](int v) {
-            if (ttid != 0 || v >= nv) return;
-            const int4 e = list[v];
-            const int h = e.x % a.Hv, kh = h / (a.Hv / a.Hk);
-            uint64_t *qbar = bars + B_QFULL + team;
-            gdn::mbar_arrive_expect_tx(qbar, 8 * kQKBox);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                gdn::tma_load_2d(bt_t + c * kBChunk, &xmap, a.Hk * D + kh * D + 32 * c, e.y, qbar);
-                gdn::tma_load_2d(bt_t + c * kBChunk + kQKBox, &xmap, kh * D + 32 * c, e.y, qbar);
-            }
-            ++qk_issued;
-        };
-        issue_qk(team);
+        // the item's q/k rows (in B) and v rows (in the team's v tile) are rows
+        // n0 .. n0 + 15; rows past the sequence's last node belong to the next
+        // sequence, or are zero-filled past the tensor: they only feed outputs
+        // that are never written
+        int v_issued = 0;
         // test hook: team 0 of CTA 0 waits on a barrier that nothing completes,
         // so the wait runs out, and every role drains and leaves
         if (a.stall_ns && blockIdx.x == 0 && team == 0 &&
@@ -835,19 +846,18 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             const int4 e = list[v];
             const int h = e.x % a.Hv, n0 = e.y, lc = e.z;
             const int voff = 2 * a.Hk * D + h * D;
+            const int bb = v % NB;
+            unsigned char *bt_t = sb + BT + bb * kBTeam;
             int p = p_nx;
             const float bv = bv_nx, av = av_nx, dtb = dtb_nx, Ah = ah_nx;
-            // the previous item's output stores have read the tiles; the team's
-            // previous epilogue has finished reading the small area
-            if (ttid == 0) gdn::bulk_wait_read0();
+            // the team's previous epilogue has finished reading the small area
+            // and the v tile
             team_sync(team);
-            // the item's 16 v rows by TMA into the u tile (free now: its last
-            // store has read it); the epilogue reads them from there and each
-            // thread writes its u over exactly the entries it read
+            // the item's 16 v rows by TMA into the team's v tile
             if (ttid == 0) {
                 uint64_t *vb = bars + B_VFULL + team;
                 gdn::mbar_arrive_expect_tx(vb, kSeg * D * 4);
-                gdn::tma_load_2d(stg_u, &vmap, voff, n0, vb);
+                gdn::tma_load_2d(stg_v, &vmap, voff, n0, vb);
                 ++v_issued;
             }
 
@@ -953,35 +963,25 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
             }
             team_sync(team);  // coefficients of every node are in
 
-            // ---- D: the replay rows' k^ and this thread's v ----------------------
-            // replay: k^ of this warp's nodes, from B's raw rows
-            const bool full = lc == kSeg;  // all 16 rows of the tiles belong to this sequence
+            // ---- D: the replay rows' k^, from B's raw rows ----------------------
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int t = tw + 4 * m;
                 if (t < lc && staged) {
                     const float4 kh = scale4(*reinterpret_cast<const float4 *>(bt_t + sw_off(t, 4 * lane, kBChunk)),
                                              rk_s[t]);
-                    if (full)
-                        *reinterpret_cast<float4 *>(stg_k + t * D + 4 * lane) = kh;
-                    else
-                        *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride +
-                                                    4 * lane) = kh;
+                    *reinterpret_cast<float4 *>(a.replay + ((n0 + t) * int64_t(a.Hv) + h) * a.rstride + 4 * lane) =
+                        kh;
                 }
             }
-            team_sync(team);  // B is no longer read
+            team_sync(team);  // B is no longer read by the team
+            if (ttid == 0) mbar_arrive(bars + B_BFREE + bb);
 
             // ---- E: per row, r = beta (v - Gamma S0 k^), u = T r, o = Gamma S0 q^ + W r
             // warp-uniform: tcgen05.ld is warp-collective
             const bool ready = __all_sync(0xffffffffu,
                                           wait_or_abort(bars + B_ACCFULL + team, uint32_t(ut & 1), abort_flag) &&
                                               wait_or_abort(bars + B_VFULL + team, uint32_t(ut & 1), abort_flag));
-            if (ready) {
-                // the products are done and the team has finished reading B: its
-                // next q/k rows may land there while this epilogue runs
-                gdn::fence_proxy_async_smem();
-                issue_qk(v + 2);
-            }
             prefetch(v + 2);
             if (ready) {
                 gdn::tc_fence_after_sync();
@@ -1009,7 +1009,7 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 // Then o = Gamma S0 q^ + CQ u the same way.
                 float vreg[kSeg];
 #pragma unroll
-                for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? stg_u[t * D + row] : 0.f;
+                for (int t = 0; t < kSeg; ++t) vreg[t] = t < lc ? stg_v[t * D + row] : 0.f;
                 uint64_t up[kSeg / 2], op[kSeg / 2];
 #pragma unroll
                 for (int p2 = 0; p2 < kSeg / 2; ++p2) {
@@ -1048,42 +1048,20 @@ __global__ void __launch_bounds__(wsv::kThreadsWS, 1)
                 float *orow = a.o + (int64_t(n0) * a.Hv + h) * D + row;
                 float *urow = a.replay + (int64_t(n0) * a.Hv + h) * a.rstride + D + row;
                 const int64_t ostep = int64_t(a.Hv) * D, ustep = int64_t(a.Hv) * a.rstride;
-                if (full) {
+                // a warp's 32 rows are contiguous: each store is one 128-byte line
 #pragma unroll
-                    for (int t = 0; t < kSeg; ++t) {
+                for (int t = 0; t < kSeg; ++t) {
+                    if (t < lc) {
                         const float2 o01 = gdn::f2unpack(op[t / 2]), u01 = gdn::f2unpack(up[t / 2]);
-                        stg_o[t * D + row] = (t & 1) ? o01.y : o01.x;
-                        stg_u[t * D + row] = (t & 1) ? u01.y : u01.x;
+                        orow[t * ostep] = (t & 1) ? o01.y : o01.x;
+                        urow[t * ustep] = (t & 1) ? u01.y : u01.x;
                     }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < kSeg; ++t) {
-                        if (t < lc) {
-                            const float2 o01 = gdn::f2unpack(op[t / 2]), u01 = gdn::f2unpack(up[t / 2]);
-                            orow[t * ostep] = (t & 1) ? o01.y : o01.x;
-                            urow[t * ustep] = (t & 1) ? u01.y : u01.x;
-                        }
-                    }
-                }
-            }
-            // a full item's o, k^ and u tiles leave by three TMA stores
-            if (full) {
-                gdn::fence_proxy_async_smem();
-                team_sync(team);
-                if (ttid == 0 && staged) {
-                    gdn::tma_store_3d(&omap, stg_o, 0, h, n0);
-                    gdn::tma_store_3d(&rmap, stg_k, 0, h, n0);
-                    gdn::tma_store_3d(&rmap, stg_u, D, h, n0);
-                    gdn::bulk_commit_group();
                 }
             }
             // after a timeout the team keeps looping (every wait now returns at
             // once) so that all four warps meet at each team barrier
         }
-        if (ttid == 0) gdn::bulk_wait0();  // the last output stores are complete
-        // after a timeout, a q/k or v copy may still be in flight: wait for it (bounded)
-        if (*abort_flag && qk_issued > 0)
-            gdn::mbar_wait_bounded(bars + B_QFULL + team, uint32_t((qk_issued - 1) & 1));
+        // after a timeout, a v copy may still be in flight: wait for it (bounded)
         if (*abort_flag && v_issued > 0)
             gdn::mbar_wait_bounded(bars + B_VFULL + team, uint32_t((v_issued - 1) & 1));
     }
@@ -1163,31 +1141,14 @@ int encode_xc_map(CUtensorMap *map, const float *xc, int64_t N, int64_t C, uint3
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
 }
 
-// An output tensor [N][H_v][row_floats] (o, or the replay rows) for TMA stores
-// of [16 nodes][1 head][d floats] tiles, unswizzled.
-int encode_out_map(CUtensorMap *map, float *base, int64_t N, int64_t Hv, int64_t row_floats, int D) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return GDN_ERR_TMA;
-    cuuint64_t gdim[3] = {cuuint64_t(row_floats), cuuint64_t(Hv), cuuint64_t(N)};
-    cuuint64_t gstride[2] = {cuuint64_t(row_floats) * 4, cuuint64_t(Hv * row_floats) * 4};
-    cuuint32_t box[3] = {cuuint32_t(D), 1, 16};
-    cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_TMA;
-}
-
 std::atomic<uint64_t> g_stall_ns{0};
 
 int launch_tc(const CUtensorMap &map, const VerifyArgs &a_in, cudaStream_t st) {
     VerifyArgs a = a_in;
     a.stall_ns = gdn::take_test_stall_ns();
-    CUtensorMap xmap, vmap, omap, rmap;
+    CUtensorMap xmap, vmap;
     if (int rc = encode_xc_map(&xmap, a.xc, a.N, a.C, 16, 32, true)) return rc;
     if (int rc = encode_xc_map(&vmap, a.xc, a.N, a.C, 16, wsv::D, false)) return rc;
-    if (int rc = encode_out_map(&omap, a.o, a.N, a.Hv, wsv::D, wsv::D)) return rc;
-    if (int rc = encode_out_map(&rmap, a.replay, a.N, a.Hv, a.rstride, wsv::D)) return rc;
     auto k = tree_verify_ws_kernel;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(wsv::BYTES)) != cudaSuccess)
         return GDN_ERR_LAUNCH;
@@ -1196,7 +1157,7 @@ int launch_tc(const CUtensorMap &map, const VerifyArgs &a_in, cudaStream_t st) {
     if (sms <= 0) return GDN_ERR_LAUNCH;
     // one CTA per SM, each with at most kMaxItems items (more CTAs queue behind)
     int64_t grid = std::max<int64_t>(std::min<int64_t>(items, sms), (items + wsv::kMaxItems - 1) / wsv::kMaxItems);
-    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, vmap, omap, rmap, a) == cudaSuccess
+    return gdn::launch_pdl(k, dim3(unsigned(grid)), dim3(wsv::kThreadsWS), wsv::BYTES, st, map, xmap, vmap, a) == cudaSuccess
                ? GDN_OK
                : GDN_ERR_LAUNCH;
 }
