@@ -719,22 +719,29 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                 gdn::tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) arrive(bars + B_DFREE);
-                // o_t = q_scale (Gamma_t b_t + sum_{j<=t} CQ[t][j] u_j)
+                // ob_t = Gamma_t b_t (without q_scale)
 #pragma unroll
-                for (int t = 0; t < kChunk; ++t) {
-                    float oq = cb[C_GAM + t] * ((ar[t] + tmp[t]) * cb[C_RQ + t]);
-                    const float *cq = cb + C_CQ + t * RS;
+                for (int t = 0; t < kChunk; ++t) ar[t] = cb[C_GAM + t] * ((ar[t] + tmp[t]) * cb[C_RQ + t]);
+                // o_t = q_scale (ob_t + sum_{j<=t} CQ[t][j] u_j)
+                auto emit_o = [&](const float (&ob)[kChunk], const float (&uu)[kChunk]) {
 #pragma unroll
-                    for (int j4 = 0; j4 <= t / 4; ++j4) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(cq + 4 * j4);
-                        oq = fmaf(cv.x, u[4 * j4], oq);
-                        oq = fmaf(cv.y, u[4 * j4 + 1], oq);
-                        oq = fmaf(cv.z, u[4 * j4 + 2], oq);
-                        oq = fmaf(cv.w, u[4 * j4 + 3], oq);
+                    for (int t = 0; t < kChunk; ++t) {
+                        float oq = ob[t];
+                        const float *cq = cb + C_CQ + t * RS;
+#pragma unroll
+                        for (int j4 = 0; j4 <= t / 4; ++j4) {
+                            const float4 cv = *reinterpret_cast<const float4 *>(cq + 4 * j4);
+                            oq = fmaf(cv.x, uu[4 * j4], oq);
+                            oq = fmaf(cv.y, uu[4 * j4 + 1], oq);
+                            oq = fmaf(cv.z, uu[4 * j4 + 2], oq);
+                            oq = fmaf(cv.w, uu[4 * j4 + 3], oq);
+                        }
+                        if (t < L) a.o[((nf + t) * a.Hv + h) * D + i] = a.q_scale * oq;
                     }
-                    if (t < L) a.o[((nf + t) * a.Hv + h) * D + i] = a.q_scale * oq;
-                }
-                if (!last) {
+                };
+                if (last) {
+                    emit_o(ar, u);
+                } else {
                     // U' = gamma_{j->L-1} u_j and its lo part into tensor memory;
                     // the state scaled by Gamma_{L-1}
                     float uw[32];
@@ -744,6 +751,19 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                         uw[kChunk + j] = lo_part(uw[j]);
                     }
                     tmem_st32(tmem + lanes + TM_U, uw);
+                    // o waits until the next chunk's products can start: u and ob
+                    // rest in the fp16 product's columns, which are free from the
+                    // release of the accumulators until this chunk's S_lo is
+                    // released (the next products wait for both)
+                    {
+                        float keep[32];
+#pragma unroll
+                        for (int t = 0; t < kChunk; ++t) {
+                            keep[t] = u[t];
+                            keep[kChunk + t] = ar[t];
+                        }
+                        tmem_st32(tmem + lanes + TM_DL, keep);
+                    }
                     const float gl = cb[C_GAM + L - 1];
 #pragma unroll 1
                     for (int b = 0; b < 4; b += 2) {
@@ -787,10 +807,14 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                         gdn::tmem_ld32(tmem + lanes + TM_S + 32 * b, sv);
                         store_slo(tiles + T_SL + (b >> 1) * kSLChunk, i, b & 1, sv, sc);
                     }
+                    float ku[kChunk], kob[kChunk];
+                    gdn::tmem_ld16(tmem + lanes + TM_DL, ku);
+                    gdn::tmem_ld16(tmem + lanes + TM_DL + kChunk, kob);
                     gdn::fence_proxy_async_smem();
                     gdn::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) arrive(bars + B_SRDY);
+                    emit_o(kob, ku);
                 }
             }
         }
