@@ -59,8 +59,10 @@ def test_bad_node_offsets_and_too_many_nodes():
     assert_pools_unchanged(pools, lp)
 
 
-def test_commit_duplicate_slot_is_rejected_whole():
-    b, lp = custom_batch(14, 1, 2, 16, [5, 6, 4], accepted=[2, 3, 1])
+@pytest.mark.parametrize("d,max_nodes", [(16, None), (128, 16), (128, 64)])
+def test_commit_duplicate_slot_is_rejected_whole(d, max_nodes):
+    """At d = 128 through the streaming apply (both ring shapes)."""
+    b, lp = custom_batch(14, 1, 2, d, [5, 6, 4], accepted=[2, 3, 1], max_nodes=max_nodes)
     b.slot_map = b.slot_map.copy()
     b.slot_map[2] = b.slot_map[0]
     st, pools = status_of(b, lp)
@@ -80,9 +82,11 @@ def test_commit_bad_accepted(acc):
     assert_pools_unchanged(pools, lp)
 
 
-def test_commit_refuses_after_an_earlier_error():
-    """A non-zero status on entry (e.g. left by verify) blocks the commit."""
-    b, lp = custom_batch(16, 1, 2, 16, [5, 6], accepted=[2, 3])
+@pytest.mark.parametrize("d,max_nodes", [(16, None), (128, 16), (128, 64)])
+def test_commit_refuses_after_an_earlier_error(d, max_nodes):
+    """A non-zero status on entry (e.g. left by verify) blocks the commit; at
+    d = 128 through the streaming apply (both ring shapes)."""
+    b, lp = custom_batch(16, 1, 2, d, [5, 6], accepted=[2, 3], max_nodes=max_nodes)
     pools = GpuPools(lp.ssm, lp.conv_hist)
     g = run_gpu(b, pools, commit=False)
     assert g.status == 0

@@ -134,6 +134,26 @@ def test_zero_length_commits_are_identity():
     run_edge(b, lp)
 
 
+def test_commit_many_units_per_cta():
+    """80 sequences x 32 heads x 2 half-heads = 5120 commit units at d = 128:
+    more than 32 per CTA, so the commit's producers scan more than one chunk of
+    their units; about a third of the sequences commit nothing."""
+    rng = np.random.default_rng(701)
+    sizes = [int(x) for x in rng.integers(1, 6, size=80)]
+    acc = [-1 if rng.random() < 0.3 else int(rng.integers(0, n)) for n in sizes]
+    b, lp = custom_batch(701, 16, 32, 128, sizes, accepted=acc, max_nodes=16, P=81)
+    run_edge(b, lp)
+
+
+def test_commit_full_length_paths():
+    """Accepted paths of 64, 33, 32, 17 and 1 nodes at d = 128: the commit's long
+    ring takes the first 32 entries with the tile and the rest, up to 32, in
+    the tile's space once the tile is in registers."""
+    sizes = [64, 33, 32, 17, 1]
+    b, lp = custom_batch(702, 2, 4, 128, sizes, kind="chain", max_nodes=64, accepted=[n - 1 for n in sizes])
+    run_edge(b, lp)
+
+
 def test_verify_leaves_pools_and_is_deterministic():
     b, lp = custom_batch(800, 2, 4, 128, [16, 16, 12])
     pools = GpuPools(lp.ssm, lp.conv_hist)
