@@ -66,8 +66,8 @@ constexpr int S_GR = S_CK + 16 * RS;     // [16][32] raw k_j . [k | q]_c
 constexpr int S_QQ = S_GR + 16 * 32;     // [16] raw q_t . q_t
 constexpr int S_BETA = S_QQ + 16, S_DEC = S_BETA + 16;
 constexpr int S_CB = S_DEC + 16;         // two buffers (chunk parity) of what the epilogue reads:
-constexpr int C_TR = 0;                  //   [16][RS] T[t][j]
-constexpr int C_CQ = C_TR + 16 * RS;     //   [16][RS] CQ[t][j] (without q_scale)
+constexpr int C_TR = 0;                  //   [16][RS] T transposed: row j holds T[t][j] over t
+constexpr int C_CQ = C_TR + 16 * RS;     //   [16][RS] CQ transposed (without q_scale)
 constexpr int C_GAM = C_CQ + 16 * RS;    //   [16] Gamma_t
 constexpr int C_W = C_GAM + 16;          //   [16] gamma_{j->L-1}
 constexpr int C_RK = C_W + 16;           //   [16] 1/|k_t|
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                         cq = gm * (fw[S_GR + j * 32 + kChunk + t] * (rkj * cb[C_RQ + t]));
                     }
                     fw[S_CK + t * RS + j] = ck;
-                    cb[C_CQ + t * RS + j] = cq;
+                    cb[C_CQ + j * RS + t] = cq;
                 }
                 prep_sync();
                 if (warp == kPrep0) {
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                             for (int s2 = 0; s2 < t; ++s2) acc = fmaf(fw[S_CK + t * RS + s2], tc[s2], acc);
                             const float b = fw[S_BETA + t];
                             tc[t] = t == j ? b : (t > j ? -b * acc : 0.f);
-                            cb[C_TR + t * RS + j] = tc[t];
+                            cb[C_TR + j * RS + t] = tc[t];
                         }
                     }
                 } else if (landed) {
@@ -693,23 +693,34 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
                     const float aj = (ar[j] + tmp[j]) * cb[C_RK + j];
                     vr[j] = j < L ? vr[j] - cb[C_GAM + j] * aj : 0.f;
                 }
-                // u = T e
+                // u = T e, column by column (j ascending, as packed node pairs;
+                // T[t][j] is zero for t < j)
                 float u[kChunk];
+                {
+                    uint64_t up[kChunk / 2];
 #pragma unroll
-                for (int t = 0; t < kChunk; ++t) {
-                    float acc = 0.f;
-                    const float *tr = cb + C_TR + t * RS;
+                    for (int q = 0; q < kChunk / 2; ++q) up[q] = gdn::f2pack(0.f, 0.f);
 #pragma unroll
-                    for (int j4 = 0; j4 <= t / 4; ++j4) {
-                        const float4 tv = *reinterpret_cast<const float4 *>(tr + 4 * j4);
-                        acc = fmaf(tv.x, vr[4 * j4], acc);
-                        acc = fmaf(tv.y, vr[4 * j4 + 1], acc);
-                        acc = fmaf(tv.z, vr[4 * j4 + 2], acc);
-                        acc = fmaf(tv.w, vr[4 * j4 + 3], acc);
+                    for (int j = 0; j < kChunk; ++j) {
+                        const uint64_t ee = gdn::f2pack(vr[j], vr[j]);
+                        const ulonglong2 *col = reinterpret_cast<const ulonglong2 *>(cb + C_TR + j * RS);
+#pragma unroll
+                        for (int q4 = j / 4; q4 < kChunk / 4; ++q4) {
+                            const ulonglong2 c = col[q4];
+                            up[2 * q4] = gdn::fma2(c.x, ee, up[2 * q4]);
+                            up[2 * q4 + 1] = gdn::fma2(c.y, ee, up[2 * q4 + 1]);
+                        }
                     }
-                    u[t] = acc;
-                    if (t < L) a.replay[((nf + t) * a.Hv + h) * a.rstride + D + i] = acc;
+#pragma unroll
+                    for (int q = 0; q < kChunk / 2; ++q) {
+                        const float2 uv = gdn::f2unpack(up[q]);
+                        u[2 * q] = uv.x;
+                        u[2 * q + 1] = uv.y;
+                    }
                 }
+#pragma unroll
+                for (int t = 0; t < kChunk; ++t)
+                    if (t < L) a.replay[((nf + t) * a.Hv + h) * a.rstride + D + i] = u[t];
                 // b_t (raw q) the same way, then the accumulators are free
                 gdn::tmem_ld16(tmem + lanes + TM_DL + 16, ar);
                 gdn::tmem_ld16(tmem + lanes + TM_DH + 48, tmp);
@@ -723,20 +734,26 @@ __global__ void __launch_bounds__(ctc::kThreads, 2)
 #pragma unroll
                 for (int t = 0; t < kChunk; ++t) ar[t] = cb[C_GAM + t] * ((ar[t] + tmp[t]) * cb[C_RQ + t]);
                 // o_t = q_scale (ob_t + sum_{j<=t} CQ[t][j] u_j)
+                // (column by column as for u; CQ[t][j] is zero for t < j)
                 auto emit_o = [&](const float (&ob)[kChunk], const float (&uu)[kChunk]) {
+                    uint64_t op[kChunk / 2];
+#pragma unroll
+                    for (int q = 0; q < kChunk / 2; ++q) op[q] = gdn::f2pack(ob[2 * q], ob[2 * q + 1]);
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        const uint64_t uj = gdn::f2pack(uu[j], uu[j]);
+                        const ulonglong2 *col = reinterpret_cast<const ulonglong2 *>(cb + C_CQ + j * RS);
+#pragma unroll
+                        for (int q4 = j / 4; q4 < kChunk / 4; ++q4) {
+                            const ulonglong2 c = col[q4];
+                            op[2 * q4] = gdn::fma2(c.x, uj, op[2 * q4]);
+                            op[2 * q4 + 1] = gdn::fma2(c.y, uj, op[2 * q4 + 1]);
+                        }
+                    }
 #pragma unroll
                     for (int t = 0; t < kChunk; ++t) {
-                        float oq = ob[t];
-                        const float *cq = cb + C_CQ + t * RS;
-#pragma unroll
-                        for (int j4 = 0; j4 <= t / 4; ++j4) {
-                            const float4 cv = *reinterpret_cast<const float4 *>(cq + 4 * j4);
-                            oq = fmaf(cv.x, uu[4 * j4], oq);
-                            oq = fmaf(cv.y, uu[4 * j4 + 1], oq);
-                            oq = fmaf(cv.z, uu[4 * j4 + 2], oq);
-                            oq = fmaf(cv.w, uu[4 * j4 + 3], oq);
-                        }
-                        if (t < L) a.o[((nf + t) * a.Hv + h) * D + i] = a.q_scale * oq;
+                        const float2 ov = gdn::f2unpack(op[t / 2]);
+                        if (t < L) a.o[((nf + t) * a.Hv + h) * D + i] = a.q_scale * ((t & 1) ? ov.y : ov.x);
                     }
                 };
                 if (last) {
