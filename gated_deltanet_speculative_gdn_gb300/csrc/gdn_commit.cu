@@ -14,15 +14,16 @@
 //  preflight  one warp per sequence: node range, accepted node, the parent walk
 //             (parents held in two registers per lane, walked by shuffles) and
 //             slot uniqueness among committing sequences.  Writes *status.
-//  apply      CTAs of 32 state rows of one (value head, sequence); do nothing
-//             unless *status is zero.  The path's replay rows are applied in
-//             closed form
+//  apply      does nothing unless *status is zero.  The path's replay rows are
+//             applied in closed form
 //                 S = Gamma S0 + sum_j c_j u_j k_j^T,   c_j = prod of decays after j
-//             which equals applying S <- decay_j S + u_j k_j^T root first.  The
-//             state rows are held in registers (coalesced 128-bit loads and
-//             stores), the path's replay rows are staged in shared memory, and
-//             the CTA also copies its share of the accepted node's window into
-//             the slot's conv history.
+//             which equals applying S <- decay_j S + u_j k_j^T root first, and
+//             the accepted node's window is copied into the slot's conv
+//             history.  d = 128: a persistent kernel streaming 64-row units
+//             through a ring of bulk copies (commit_stream_kernel, below);
+//             d < 128: CTAs of 32 state rows of one (value head, sequence) that
+//             hold the rows in registers and stage the path's replay rows in
+//             shared memory (commit_apply_kernel).
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_tma.h"
