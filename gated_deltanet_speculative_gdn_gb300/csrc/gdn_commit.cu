@@ -463,6 +463,20 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
         const bool failed = abort_flag[1] != 0;
         if (failed) u = -1;
         while (u >= 0 && ok) {
+            const int m = q.m;
+            // the stage's previous unit is done with
+            if (!__all_sync(all, nu == 0 || wait_or_abort(empty + p, uint32_t((nu - 1) & 1), abort_flag))) {
+                ok = false;
+                break;
+            }
+            ++nu;
+            // the tile first (its index inputs are known): it travels while the
+            // decays are read; the phase completes only at the arrival below
+            if (m && lane == 0) {
+                gdn::mbar_expect_tx(fb, kTileBytes);
+                gdn::bulk_load(stage, a.ssm + ((int64_t(q.slot) * a.Hv + q.h) * D + kUnitRows * q.half) * D,
+                               kTileBytes, fb);
+            }
             // coefficient of leaf-first entry i = product of the decays of entries 0 .. i-1
             const float *row0 = a.replay + (int64_t(q.n0) * a.Hv + q.h) * a.rstride;
             const float d_lo = q.m && q.node_lo >= 0 ? __ldg(row0 + q.node_lo * rnode + 2 * D) : 1.0f;
@@ -484,13 +498,6 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
             }
             c_hi *= tot_lo;
             const float gam = tot_lo * __shfl_sync(all, x_hi, 31);
-            const int m = q.m;
-            // the stage's previous unit is done with
-            if (!__all_sync(all, nu == 0 || wait_or_abort(empty + p, uint32_t((nu - 1) & 1), abort_flag))) {
-                ok = false;
-                break;
-            }
-            ++nu;
             if (lane < m) {
                 sa[SM_COEF + lane] = __float_as_int(c_lo);
                 sa[SM_NODE + lane] = q.node_lo;
@@ -507,14 +514,11 @@ __global__ void __launch_bounds__(R::kThreads, 1) commit_stream_kernel(const Com
             }
             __threadfence_block();
             __syncwarp();
-            // phase 1: the tile and the first kEntries entries, root first
+            // phase 1: the tile (above) and the first kEntries entries, root first
             const int cnt = min(m, kEntries), cnt2 = m - cnt;
-            if (lane == 0) gdn::mbar_arrive_expect_tx(fb, m ? kTileBytes + cnt * kEntryBytes : 0);
+            if (lane == 0) gdn::mbar_arrive_expect_tx(fb, cnt * kEntryBytes);
             ++fph;
             __syncwarp();
-            if (m && lane == 0)
-                gdn::bulk_load(stage, a.ssm + ((int64_t(q.slot) * a.Hv + q.h) * D + kUnitRows * q.half) * D,
-                               kTileBytes, fb);
             if (lane < cnt) {
                 const float *rr = row0 + sa[SM_NODE + m - 1 - lane] * rnode;
                 float *dst = ent + lane * kEntryFloats;
