@@ -268,9 +268,40 @@ def ncu_traffic(kernel: str, variant: str):
         return None
 
 
+class Ranks:
+    """The host side of a multi-process run: one process per GPU, each an
+    independent replica of the workload (no data-path exchange).  `barrier`
+    lines the ranks up around a timed region, `max` takes a per-rank figure's
+    maximum over the ranks, and only rank 0 reports.  With one process every
+    method is local.  The process group is NCCL on GPUs; the tests use gloo."""
+
+    def __init__(self, dist=None, device=None):
+        self.dist = dist
+        self.device = device
+        self.rank = dist.get_rank() if dist is not None else 0
+        self.world = dist.get_world_size() if dist is not None else 1
+
+    @property
+    def main(self) -> bool:
+        return self.rank == 0
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, values):
+        if self.dist is None:
+            return [float(v) for v in values]
+        import torch
+        t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return [float(v) for v in t.tolist()]
+
+
 def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int = 0,
-                 e2e: bool = False, clocks: bool = False):
+                 e2e: bool = False, clocks: bool = False, ranks: Ranks = None):
     import torch
+    ranks = ranks or Ranks()
     compact = variant.endswith("_compact")
     sp = W.sweep_spec(variant[: -len("_compact")] if compact else variant, rounds=N_ROUNDS)
     wl = DeviceWorkload(sp, min(N_ROUNDS, max(steps + warmup, 1)), device, seed_offset, compact=compact)
@@ -287,23 +318,27 @@ def time_variant(variant: str, steps: int, warmup: int, device, seed_offset: int
         sampler.__enter__()
         time.sleep(0.3)
     torch.cuda.synchronize()
+    ranks.barrier()                                  # every rank's timed region starts together
     for i in range(steps):
         flush(i)                                     # L2 flush, outside the step's events
         wl.step((warmup + i) % nr, ev[i])
         ends[i].record()
     torch.cuda.synchronize()
+    ranks.barrier()
     # The same K steps again with events only around each whole step: events
     # between the kernels would stop a kernel's launch from overlapping the
     # previous one's tail (programmatic dependent launch), so the step time
     # comes from this pass and the per-kernel split from the one above.
     whole = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
+    ranks.barrier()
     for i in range(steps):
         flush(i)
         whole[i][0].record()
         wl.step((warmup + i) % nr)
         whole[i][1].record()
     torch.cuda.synchronize()
+    ranks.barrier()
     if sampler:
         sampler.__exit__()
     assert int(wl.status.item()) == 0, wl.G.gdn_status_str(int(wl.status.item()))
@@ -704,13 +739,16 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
+    ranks = Ranks(dist, device)
 
     variants = (list(W.SWEEP_VARIANTS) + [HEADLINE + "_compact"] if args.variants == "all"
                 else [] if args.variants in ("", "none") else args.variants.split(","))
     if HEADLINE in variants:
         variants.remove(HEADLINE)
-    head = time_variant(HEADLINE, args.steps, args.warmup, device, seed_offset=rank, e2e=True, clocks=True)
-    others = {v: time_variant(v, args.steps, args.warmup, device, seed_offset=rank) for v in variants}
+    head = time_variant(HEADLINE, args.steps, args.warmup, device, seed_offset=rank, e2e=True, clocks=True,
+                        ranks=ranks)
+    others = {v: time_variant(v, args.steps, args.warmup, device, seed_offset=rank, ranks=ranks)
+              for v in variants}
     extra = {"decode_step": time_decode(args.steps, args.warmup, device),
              "gated_rmsnorm_headline": time_gated_norm(head["wl"], args.steps, args.warmup)}
     cfg_ids = [] if args.configs in ("", "none") else [int(c) for c in args.configs.split(",")]
@@ -721,12 +759,9 @@ def main():
     step_ms = statistics.mean(head["step_ms"])
     e2e_ms = head["e2e"]["ms_per_step"]
     e2e_ov_ms = head["e2e_overlapped"]["ms_per_step"]
-    if dist is not None:
-        t = torch.tensor([step_ms, e2e_ms, e2e_ov_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms, e2e_ov_ms = float(t[0]), float(t[1]), float(t[2])
-        dist.barrier()
-    if rank != 0:
+    step_ms, e2e_ms, e2e_ov_ms = ranks.max([step_ms, e2e_ms, e2e_ov_ms])
+    ranks.barrier()
+    if not ranks.main:
         if dist is not None:
             dist.destroy_process_group()
         return
